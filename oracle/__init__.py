@@ -1,0 +1,255 @@
+"""CPU oracle for the batched grouped-masked block-FP8 MoE expert forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (``moe_expert_layer_prepare_gb300``) never imports it, and the two
+share no code: this file only marshals numpy arrays into the plain C oracle in
+``moe_oracle.c``, which restates the pages' steps S1-S8:
+
+* vllm.model_executor.layers.fused_moe.prepare_megamoe -- ``_quantize_fp8_groups``
+  (S1 e4m3, S2 group scale, S3 quantise), ``_pack_bytes`` (S4),
+  ``_store_topk`` / ``_eplb_kernel_args`` / ``prepare_megamoe_inputs`` (S5).
+* vllm.model_executor.layers.fused_moe.experts.fused_humming_moe --
+  ``BatchedHummingGroupedExperts.apply`` and ``HummingExpertsBase.get_buffer_metas``
+  (S6 batched layout, S7 GEMMs + SiLU-and-mul + requant), ``moe_fused_mul_sum`` /
+  ``TopKWeightAndReduceDelegate`` (S8 weighted reduce).
+
+Parity unpinned: the slot order inside an expert is the dispatch's choice (the
+oracle takes (token, k) order); last-ulp differences between the CUDA ``expf``
+and the C library ``exp`` are covered by tolerance only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", f"liboracle_{platform.machine()}.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle (gcc, -O2, OpenMP, no fast-math, no FP contraction)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+        lib.orc_abi_version.restype = i32
+        lib.orc_num_threads.restype = i32
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_e4m3_encode.argtypes = [f32]
+        lib.orc_e4m3_decode.restype = f32
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_bf16_from_f64.restype = ctypes.c_uint16
+        lib.orc_bf16_from_f64.argtypes = [ctypes.c_double]
+        lib.orc_group_scale.restype = None
+        lib.orc_group_scale.argtypes = [f32, i32, ctypes.POINTER(ctypes.c_uint32),
+                                        ctypes.POINTER(f32)]
+        lib.orc_prepare_inputs.restype = i32
+        lib.orc_prepare_inputs.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32, vp, vp,
+                                           vp, vp, vp, i64, i64, vp, vp, i64, i32, i64]
+        lib.orc_dispatch.restype = i32
+        lib.orc_dispatch.argtypes = [i64, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, vp]
+        lib.orc_w13_rows.restype = None
+        lib.orc_w13_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_w2_rows.restype = None
+        lib.orc_w2_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp]
+        lib.orc_topk_reduce.restype = None
+        lib.orc_topk_reduce.argtypes = [i64, i64, i64, i64, vp, vp, vp, vp, vp]
+        _lib = lib
+        return lib
+
+
+def _p(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+# --------------------------------------------------------------------------- S1
+def e4m3_encode(v: float) -> int:
+    return int(_load().orc_e4m3_encode(float(v)))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(_load().orc_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_decode_table() -> np.ndarray:
+    """fp32 value of each of the 256 codes (NaN for 0x7F / 0xFF)."""
+    return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float32)
+
+
+def e4m3_encode_array(v: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(v, dtype=np.float32).ravel()
+    return np.array([lib.orc_e4m3_encode(float(x)) for x in flat], dtype=np.uint8).reshape(
+        np.shape(v))
+
+
+def bf16_from_f64(v: float) -> int:
+    return int(_load().orc_bf16_from_f64(float(v)))
+
+
+# --------------------------------------------------------------------------- S2
+def group_scale(amax: float, ue8m0: bool = True):
+    """Return (code, qs): UE8M0 exponent byte (or fp32 bits) and the quant scale."""
+    code = ctypes.c_uint32()
+    qs = ctypes.c_float()
+    _load().orc_group_scale(float(amax), 1 if ue8m0 else 0, ctypes.byref(code), ctypes.byref(qs))
+    return int(code.value), float(qs.value)
+
+
+# ----------------------------------------------------------------------- S1-S5
+def prepare_inputs(hidden_bf16_bits, topk_ids, topk_weights, is_padding=None, sf_mode=1,
+                   l2p=None, replica_count=None, num_physical=0, record_enabled=False,
+                   num_unpadded=None):
+    """Token-order staging.  Returns dict(x, x_sf, ids, weights, load)."""
+    lib = _load()
+    hidden = _c(hidden_bf16_bits, np.uint16)
+    T, K = hidden.shape
+    ids_is_64 = np.asarray(topk_ids).dtype == np.int64
+    ids = _c(topk_ids, np.int64 if ids_is_64 else np.int32)
+    top_k = ids.shape[1] if ids.ndim == 2 else 0
+    w = _c(topk_weights, np.float32)
+    pad = None if is_padding is None else _c(is_padding, np.uint8)
+    G = K // 128
+    x = np.zeros((T, K), np.uint8)
+    x_sf = (np.zeros((T, (G + 3) // 4), np.int32) if sf_mode == 1
+            else np.zeros((T, G), np.float32))
+    ids_out = np.zeros((T, top_k), np.int64)
+    w_out = np.zeros((T, top_k), np.float32)
+    l2p_c = None if l2p is None else _c(l2p, np.int32)
+    rc = None if replica_count is None else _c(replica_count, np.int32)
+    load = np.zeros(max(int(num_physical), 1), np.int32) if l2p is not None else None
+    st = lib.orc_prepare_inputs(
+        T, K, top_k, _p(hidden), _p(ids), int(ids_is_64), _p(w), _p(pad), int(sf_mode),
+        _p(x), _p(x_sf), _p(ids_out), _p(w_out), _p(l2p_c),
+        0 if l2p_c is None else l2p_c.shape[0], 0 if l2p_c is None else l2p_c.shape[1],
+        _p(rc), _p(load), int(num_physical), int(bool(record_enabled)),
+        T if num_unpadded is None else int(num_unpadded))
+    if st != 0:
+        raise ValueError(f"oracle staging rejected the shapes (status {st})")
+    return dict(x=x, x_sf=x_sf, ids=ids_out, weights=w_out,
+                load=None if load is None else load[:int(num_physical)])
+
+
+# --------------------------------------------------------------------------- S6
+def dispatch(ids, x, x_sf_words, E, M_max, copy_rows=True):
+    """Batched layout.  Returns dict(expert_num_tokens, route_slot, x_b, sf_b, status)."""
+    lib = _load()
+    ids = _c(ids, np.int64)
+    T, top_k = ids.shape
+    x = _c(x, np.uint8)
+    K = x.shape[1]
+    sfw = _c(x_sf_words, np.int32)
+    W = sfw.shape[1]
+    ent = np.zeros(E, np.int32)
+    slot = np.zeros((T, top_k), np.int32)
+    x_b = np.zeros((E * M_max, K), np.uint8) if copy_rows else None
+    sf_b = np.zeros((E * M_max, W), np.int32) if copy_rows else None
+    st = lib.orc_dispatch(T, top_k, K, _p(ids), _p(x), _p(sfw), E, M_max, _p(ent), _p(slot),
+                          _p(x_b), _p(sf_b))
+    return dict(expert_num_tokens=ent, route_slot=slot, x_b=x_b, sf_b=sf_b, status=int(st))
+
+
+# --------------------------------------------------------------------------- S7
+def valid_rows(expert_num_tokens, M_max):
+    ent = np.asarray(expert_num_tokens)
+    return np.concatenate([np.arange(n, dtype=np.int64) + e * M_max
+                           for e, n in enumerate(ent)] + [np.zeros(0, np.int64)])
+
+
+def w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h=False):
+    """w13 GEMM + SiLU-and-mul + requant for the given global rows.
+
+    Returns (h, y_q, y_sf) as full-size arrays [E*M_max, .]; only `rows` are set.
+    """
+    lib = _load()
+    rows = _c(rows, np.int64)
+    x_b = _c(x_b, np.uint8)
+    R = x_b.shape[0]
+    a_sf = _c(a_sf, np.int32)
+    w13 = _c(w13, np.uint8)
+    w13_s = _c(w13_s, np.float32)
+    Gn = N // 128
+    h = np.zeros((R, 2 * N), np.uint16) if want_h else None
+    y_q = np.zeros((R, N), np.uint8)
+    y_sf = np.zeros((R, (Gn + 3) // 4), np.int32)
+    lib.orc_w13_rows(rows.size, _p(rows), M_max, K, N, _p(x_b), _p(a_sf), _p(w13), _p(w13_s),
+                     _p(h), _p(y_q), _p(y_sf))
+    return h, y_q, y_sf
+
+
+def w2_rows(rows, M_max, K, N, y_q, y_sf, w2, w2_s):
+    """w2 GEMM for the given global rows; returns bf16 bits [E*M_max, K]."""
+    lib = _load()
+    rows = _c(rows, np.int64)
+    y_q = _c(y_q, np.uint8)
+    y_sf = _c(y_sf, np.int32)
+    w2 = _c(w2, np.uint8)
+    w2_s = _c(w2_s, np.float32)
+    out_b = np.zeros((y_q.shape[0], K), np.uint16)
+    lib.orc_w2_rows(rows.size, _p(rows), M_max, K, N, _p(y_q), _p(y_sf), _p(w2), _p(w2_s),
+                    _p(out_b))
+    return out_b
+
+
+# --------------------------------------------------------------------------- S8
+def topk_reduce(out_b_bits, ids, route_slot, weights, M_max):
+    lib = _load()
+    out_b = _c(out_b_bits, np.uint16)
+    ids = _c(ids, np.int64)
+    slot = _c(route_slot, np.int32)
+    w = _c(weights, np.float32)
+    T, top_k = ids.shape
+    K = out_b.shape[-1]
+    out = np.zeros((T, K), np.uint16)
+    lib.orc_topk_reduce(T, top_k, K, M_max, _p(out_b), _p(ids), _p(slot), _p(w), _p(out))
+    return out
+
+
+# ----------------------------------------------------------------- whole path
+def forward(hidden_bf16_bits, topk_ids, topk_weights, w13, w13_s, w2, w2_s, E, M_max, N,
+            is_padding=None, eplb=None, rows=None, want_h=False):
+    """S1-S8 end to end.  `rows` (global batched rows) restricts S7; default all."""
+    K = hidden_bf16_bits.shape[1]
+    eplb = eplb or {}
+    st = prepare_inputs(hidden_bf16_bits, topk_ids, topk_weights, is_padding=is_padding,
+                        sf_mode=1, **eplb)
+    d = dispatch(st["ids"], st["x"], st["x_sf"], E, M_max)
+    if rows is None:
+        rows = valid_rows(d["expert_num_tokens"], M_max)
+    h, y_q, y_sf = w13_rows(rows, M_max, K, N, d["x_b"], d["sf_b"], w13, w13_s, want_h=want_h)
+    out_b = w2_rows(rows, M_max, K, N, y_q, y_sf, w2, w2_s)
+    out = topk_reduce(out_b, st["ids"], d["route_slot"], st["weights"], M_max)
+    return dict(staging=st, dispatch=d, rows=rows, h=h, y_q=y_q, y_sf=y_sf, out_b=out_b,
+                out=out)
