@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark of the batched grouped-masked block-FP8 MoE expert layer on GB300.
+
+One step = the whole path over one batch of synthetic input:
+moe_prepare_inputs (staging + dispatch) -> moe_batched_experts (w13 GEMM with
+fused SiLU-and-mul requant, w2 GEMM) -> moe_topk_reduce.  The default workload
+is the Mixtral-8x7B-shaped decode layer (T=64, K=4096, N=14336, E=8, top-k 2).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME]
+
+Prints one JSON line.  `value` is TFLOP/s over valid (routed) rows; the
+staging-only workload reports GB/s instead.  Multi-GPU runs (torchrun) are
+independent replicas (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE expert-layer TFLOP/s (valid rows) & staging GB/s, % of FP8/HBM roofline, 1 GB300"
+FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral_decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-seconds", type=float, default=1.5)
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world <= 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sus=d.get("bf16_tflops_sustained", d["bf16_tflops"]), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.idx = device_index
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = ["-i", str(device_index)]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"], samples=0)
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(rows),
+                    power_w_max=max(pw) if pw else None)
+
+
+# ----------------------------------------------------------------- workload
+def build_workload(name, device):
+    from moe_expert_layer_prepare_gb300 import synthetic as syn
+    return syn.make_workload(name, weights_device=device)
+
+
+def algorithmic(wl):
+    """Valid-row FLOPs and algorithmic bytes per kernel."""
+    c = wl["cfg"]
+    T, K, N, E, k = c["T"], c["K"], c["N"], c["E"], c["top_k"]
+    ids = wl["topk_ids"].cpu().numpy()
+    pad = wl["is_padding"].cpu().numpy().astype(bool)
+    routed = ids[~pad]
+    R = int(routed.size)
+    A = int(np.unique(routed).size)
+    G, Gn = K // 128, N // 128
+    Wa, Wy = (G + 3) // 4, (Gn + 3) // 4
+    w13_bytes = A * (2 * N * K + (2 * N // 128) * G * 4) + R * (K + 4 * Wa) + R * (N + Gn) + 4 * E
+    w2_bytes = A * (K * N + (K // 128) * Gn * 4) + R * (N + 4 * Wy) + R * K * 2 + 4 * E
+    stage_bytes = T * K * 2 + T * k * 8 + T + T * K + T * 4 * Wa + T * k * 8 + T * k * 4 + \
+        R * (K + 4 * Wa) + R * 4 + E * 4
+    reduce_bytes = R * K * 2 + T * K * 2 + T * k * (8 + 4 + 4)
+    return dict(R=R, A=A, flops=6.0 * N * K * R, w13_bytes=w13_bytes, w2_bytes=w2_bytes,
+                stage_bytes=stage_bytes, reduce_bytes=reduce_bytes,
+                w13_flops=4.0 * N * K * R, w2_flops=2.0 * N * K * R)
+
+
+def run_oracle_sample(wl, n_tok, seed=0):
+    import oracle
+    oracle.build()
+    c = wl["cfg"]
+    rng = np.random.default_rng(seed)
+    pad = wl["is_padding"].cpu().numpy()
+    cand = np.nonzero(pad == 0)[0]
+    tokens = np.sort(rng.choice(cand, size=min(n_tok, cand.size), replace=False))
+
+    def weights_of(experts):
+        sel = torch.as_tensor(np.asarray(experts, np.int64))
+        return tuple(np.ascontiguousarray(wl[n][sel.to(wl[n].device)].cpu().numpy())
+                     for n in ("w13", "w13_s", "w2", "w2_s"))
+
+    bits = wl["hidden"].view(torch.int16).numpy().view(np.uint16)
+    tm = {}
+    oracle.sampled_forward(bits, wl["topk_ids"].numpy(), wl["topk_weights"].numpy(), pad,
+                           c["E"], c["M_max"], c["N"], tokens, weights_of, timings=tm)
+    return tm, oracle.num_threads(), len(tokens)
+
+
+def oracle_tokens_for(wl, seconds):
+    """Token sample size for about `seconds` of oracle wall time (estimate)."""
+    c = wl["cfg"]
+    per_route = 6.0 * c["N"] * c["K"]
+    import oracle
+    thr = max(oracle.num_threads(), 1)
+    rate = 1.2e8 * thr  # oracle fp64 FLOP/s per thread (measured order of magnitude)
+    routes = max(1, int(seconds * rate / per_route))
+    return max(1, routes // max(c["top_k"], 1))
+
+
+# ----------------------------------------------------------------- ours
+def bench_ours(args, world, rank, local):
+    from moe_expert_layer_prepare_gb300 import binding as B
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B.load()
+    name = args.config
+    wl = build_workload(name, dev)
+    c = wl["cfg"]
+    peaks = load_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    alg = algorithmic(wl) if c.get("N") else None
+
+    if c.get("N") is None:
+        return bench_staging(args, world, rank, dev, wl, peaks, flush)
+
+    layer = B.MoeLayer(c["T"], c["K"], c["N"], c["E"], c["top_k"], c["M_max"], wl["w13"],
+                       wl["w13_s"], wl["w2"], wl["w2_s"], device=dev)
+    hid, ids, wts, pad = (wl["hidden"].to(dev), wl["topk_ids"].to(dev),
+                          wl["topk_weights"].to(dev), wl["is_padding"].to(dev))
+    inter_q, inter_sf = layer.inter()
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(s)
+        layer.prepare(hid, ids, wts, pad)
+        if evs:
+            evs[1].record(s)
+        B.moe_batched_experts(layer.out_b, layer.x_b, layer.sf_b, layer.w13, layer.w13_s,
+                              layer.w2, layer.w2_s, layer.expert_num_tokens, layer.ws13,
+                              layer.ws2, valid_shape_m=layer.valid_shape_m,
+                              stages=B.MOE_STAGE_W13, device_status=layer.status)
+        if evs:
+            evs[2].record(s)
+        B.moe_batched_experts(layer.out_b, None, None, layer.w13, layer.w13_s, layer.w2,
+                              layer.w2_s, layer.expert_num_tokens, layer.ws13, layer.ws2,
+                              valid_shape_m=layer.valid_shape_m, inter_q=inter_q,
+                              inter_sf=inter_sf, stages=B.MOE_STAGE_W2,
+                              device_status=layer.status)
+        if evs:
+            evs[3].record(s)
+        layer.reduce()
+        if evs:
+            evs[4].record(s)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0, "device status set during warm-up"
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_end = time.time() + args.soak_seconds
+    while time.time() < t_end:
+        for _ in range(20):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop()
+    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+                         for i in range(K)])
+    step_ms = stage_ms.sum(axis=1)
+    ms = float(step_ms.mean())
+    ms_max = max_over_ranks(world, ms)
+    value = world * alg["flops"] / (ms_max * 1e-3) / 1e12
+    means = stage_ms.mean(axis=0)
+    w13_gbs = alg["w13_bytes"] / (means[1] * 1e-3) / 1e9
+    w13_tfs = alg["w13_flops"] / (means[1] * 1e-3) / 1e12
+    prefill = name == "deepseek_prefill"
+    if prefill:
+        peak = peaks["bf16"] * FP8_OVER_BF16
+        roof = dict(bound="tensor", achieved=round(w13_tfs, 2), peak=round(peak, 1),
+                    unit="TFLOP/s", frac=round(w13_tfs / peak, 4), traffic=None,
+                    kernel="grouped_gemm_kernel<W13>",
+                    peak_source=f"{peaks['src']} bf16 burst x {FP8_OVER_BF16} (fp8/bf16 nominal)")
+    else:
+        roof = dict(bound="hbm", achieved=round(w13_gbs, 1), peak=peaks["hbm"], unit="GB/s",
+                    frac=round(w13_gbs / peaks["hbm"], 4), traffic=None,
+                    kernel="grouped_gemm_kernel<W13>", peak_source=f"{peaks['src']} hbm_gbs")
+
+    # end to end through the public API with pinned host buffers
+    hh = wl["hidden"].pin_memory()
+    ih = wl["topk_ids"].pin_memory()
+    wh = wl["topk_weights"].pin_memory()
+    ph = wl["is_padding"].pin_memory()
+    oh = torch.empty((c["T"], c["K"]), dtype=torch.bfloat16).pin_memory()
+    for _ in range(3):
+        layer.forward_host(hh, ih, wh, ph, oh)
+    torch.cuda.synchronize()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        e_ev[i][0].record(s)
+        layer.forward_host(hh, ih, wh, ph, oh)
+        e_ev[i][1].record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(world, float(np.mean([a.elapsed_time(b) for a, b in e_ev])))
+    h2d = hh.numel() * 2 + ih.numel() * ih.element_size() + wh.numel() * 4 + ph.numel()
+    d2h = oh.numel() * 2
+    assert int(layer.status.item()) == 0, "device status set during the timed steps"
+
+    out = dict(metric=METRIC, value=round(value, 3), unit="TFLOP/s", n_gpus=world, steps=K,
+               warmup=args.warmup, ms_per_step=round(ms_max, 4), higher_is_better=True,
+               scaling="weak", vs_baseline=None, dtype="fp8e4m3 (fp32 accumulate)",
+               data="synthetic",
+               config=dict(workload=name, T=c["T"], K=c["K"], N=c["N"], E=c["E"],
+                           top_k=c["top_k"], M_max=c["M_max"], routed_rows=alg["R"],
+                           active_experts=alg["A"],
+                           l2="inputs larger than L2 and a 512 MB L2 flush before every step",
+                           parallelism=f"replicas x{world}"),
+               roofline=roof,
+               stages_ms=dict(prepare=round(means[0], 4), w13=round(means[1], 4),
+                              w2=round(means[2], 4), reduce=round(means[3], 4)),
+               stages_gbs=dict(prepare=round(alg["stage_bytes"] / means[0] / 1e6, 1),
+                               w13=round(w13_gbs, 1),
+                               w2=round(alg["w2_bytes"] / means[2] / 1e6, 1),
+                               reduce=round(alg["reduce_bytes"] / means[3] / 1e6, 1)),
+               e2e=dict(value=round(world * alg["flops"] / (e2e_ms * 1e-3) / 1e12, 3),
+                        unit="TFLOP/s", h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
+                        ms_per_step=round(e2e_ms, 4)),
+               gpu_launches=5 * K, clocks=ck)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        n_tok = oracle_tokens_for(wl, 15.0)
+        tm, thr, ntok = run_oracle_sample(wl, n_tok)
+        out["cpu_baseline"] = dict(value=round(tm["flops"] / tm["seconds"] / 1e12, 6),
+                                   unit="TFLOP/s", cores=thr, kind="oracle",
+                                   sample=f"{ntok} tokens ({tm['routes']} routes) of {name}, "
+                                          f"{tm['seconds']:.1f} s")
+    return out
+
+
+def bench_staging(args, world, rank, dev, wl, peaks, flush):
+    """staging_stress: moe_prepare_inputs alone (token order, EPLB)."""
+    from moe_expert_layer_prepare_gb300 import binding as B
+    c = wl["cfg"]
+    T, K, k = c["T"], c["K"], c["top_k"]
+    G = K // 128
+    hid = wl["hidden"].to(dev)
+    ids, wts = wl["topk_ids"].to(dev), wl["topk_weights"].to(dev)
+    x = torch.empty((T, K), dtype=torch.uint8, device=dev)
+    x_sf = torch.empty((T, (G + 3) // 4), dtype=torch.int32, device=dev)
+    io = torch.empty((T, k), dtype=torch.int64, device=dev)
+    wo = torch.empty((T, k), dtype=torch.float32, device=dev)
+    load = torch.zeros(wl["num_physical"], dtype=torch.int32, device=dev)
+    eplb = dict(logical_to_physical=wl["l2p"].to(dev), logical_replica_count=wl["replica_count"]
+                .to(dev), expert_load=load, should_record=torch.ones(1, dtype=torch.uint8,
+                                                                        device=dev),
+                num_unpadded_tokens=torch.tensor([T], dtype=torch.int32, device=dev))
+    s = torch.cuda.current_stream()
+
+    def step():
+        B.moe_prepare_inputs(hid, ids, wts, x, x_sf, io, wo, eplb=eplb)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    t_end = time.time() + args.soak_seconds
+    while time.time() < t_end:
+        for _ in range(20):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+    Ks = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Ks)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(Ks):
+        flush.zero_()
+        evs[i][0].record(s)
+        step()
+        evs[i][1].record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop()
+    ms = max_over_ranks(world, float(np.mean([a.elapsed_time(b) for a, b in evs])))
+    nbytes = T * K * 2 + T * k * 4 * 2 + T * K + T * 4 * ((G + 3) // 4) + T * k * 12 + \
+        wl["l2p"].numel() * 4 + wl["replica_count"].numel() * 4
+    gbs = world * nbytes / (ms * 1e-3) / 1e9
+    return dict(metric=METRIC, value=round(gbs, 1), unit="GB/s", n_gpus=world, steps=Ks,
+                warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="bf16->fp8e4m3 (fp32 scale math)",
+                data="synthetic",
+                config=dict(workload="staging_stress", T=T, K=K, top_k=k, experts_logical=c["E"],
+                            experts_physical=wl["num_physical"],
+                            l2="inputs larger than L2 and a 512 MB L2 flush before every step"),
+                roofline=dict(bound="hbm", achieved=round(gbs / world, 1), peak=peaks["hbm"],
+                              unit="GB/s", frac=round(gbs / world / peaks["hbm"], 4),
+                              traffic=None, kernel="quant_kernel<UE8M0,repack>"),
+                gpu_launches=Ks, clocks=ck)
+
+
+# ----------------------------------------------------------------- reference
+def bench_reference(args, world, rank):
+    """The oracle as it stands on the host cores: each step a bounded sample."""
+    if rank != 0:
+        return None
+    wl = build_workload(args.config, "cpu")
+    c = wl["cfg"]
+    if c.get("N") is None:
+        return dict(impl="reference", unavailable="the staging-only workload has no oracle "
+                    "timing leg in this harness")
+    alg = algorithmic(wl)
+    n_tok = oracle_tokens_for(wl, 2.0)
+    for _ in range(max(args.warmup, 0)):
+        run_oracle_sample(wl, n_tok, seed=1)
+    secs, flops = [], []
+    t_wall = time.time()
+    for i in range(args.steps):
+        tm, thr, ntok = run_oracle_sample(wl, n_tok, seed=100 + i)
+        secs.append(tm["seconds"])
+        flops.append(tm["flops"])
+    value = sum(flops) / sum(secs) / 1e12
+    ms = 1e3 * float(np.mean(secs))
+    del t_wall
+    return dict(metric=METRIC, value=round(value, 6), unit="TFLOP/s", n_gpus=world,
+                steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 3),
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="fp64 (oracle)",
+                data="synthetic", impl="reference",
+                config=dict(workload=args.config, T=c["T"], K=c["K"], N=c["N"], E=c["E"],
+                            top_k=c["top_k"], M_max=c["M_max"], routed_rows=alg["R"]),
+                cpu_baseline=dict(kind="oracle", cores=thr, value=round(value, 6),
+                                  sample=f"{ntok} tokens per step of {args.config}"),
+                e2e=dict(value=round(value, 6), unit="TFLOP/s", h2d_bytes_per_step=0,
+                         d2h_bytes_per_step=0))
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        out = bench_reference(args, world, rank)
+    else:
+        out = bench_ours(args, world, rank, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

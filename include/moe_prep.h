@@ -1,0 +1,259 @@
+/*
+ * moe_prep.h -- C ABI of the GB300 (sm_103a) batched grouped-masked block-FP8
+ * MoE expert forward.
+ *
+ * Three entry points make up the path:
+ *
+ *   moe_prepare_inputs   input staging: bf16 -> fp8 e4m3 with 1x128 UE8M0
+ *                        scales, top-k repack (int64 ids, fp32 weights),
+ *                        EPLB replica map, and optionally the dispatch into
+ *                        the batched [experts, max_tokens, K] layout.
+ *   moe_batched_experts  w13 gate_up GEMM masked by expert_num_tokens, fused
+ *                        SiLU-and-mul + FP8 requant, w2 down GEMM.
+ *   moe_topk_reduce      top-k weighted sum back to token order.
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise; every
+ *     output buffer is allocated by the caller; the library never allocates
+ *     device memory.
+ *   - Strides are in ELEMENTS of the tensor's own dtype.
+ *   - `stream` is a cudaStream_t passed as void*.  Work is enqueued
+ *     asynchronously; nothing synchronises the host.
+ *   - Host-checkable problems return a moe_status_t before anything is
+ *     enqueued; moe_last_error() then holds a message (thread-local).
+ *   - Problems only the device can see (an expert receiving more routes than
+ *     it has rows, a routed id outside [0, num_experts), a GEMM wait that
+ *     timed out) are OR-ed into *device_status (MOE_DEV_* bits) when the
+ *     caller passes one.  Kernels never trap.
+ */
+#ifndef MOE_PREP_H
+#define MOE_PREP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_PREP_ABI_VERSION 1
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARGUMENT = 1, /* NULL where required, negative size, bad enum */
+  MOE_ERR_SHAPE = 2,            /* a shape rule of the pages is broken */
+  MOE_ERR_UNSUPPORTED = 3,      /* a combination this library does not implement */
+  MOE_ERR_ALIGNMENT = 4,        /* pointer/stride alignment needed by vector or TMA access */
+  MOE_ERR_WORKSPACE = 5,        /* workspace missing or smaller than the size query */
+  MOE_ERR_CUDA = 6              /* a CUDA runtime call failed */
+} moe_status_t;
+
+/* Device status bits (OR-ed into *device_status). */
+#define MOE_DEV_CAPACITY 1u   /* an expert got more than max_tokens_per_expert routes */
+#define MOE_DEV_BAD_EXPERT 2u /* routed id >= num_experts / num_logical, or bad EPLB entry */
+#define MOE_DEV_TIMEOUT 4u    /* a bounded pipeline wait inside a GEMM expired */
+
+typedef enum moe_sf_mode {
+  MOE_SF_NONE = 0,         /* no quantisation: x receives a bf16 copy of hidden */
+  MOE_SF_UE8M0_PACKED = 1, /* x_sf int32 [T, ceil(G/4)]: group g is byte g%4 of word g/4 */
+  MOE_SF_FP32 = 2          /* x_sf fp32 [T, G]: the group scale amax/448 itself */
+} moe_sf_mode_t;
+
+typedef enum moe_ids_dtype { MOE_IDS_INT32 = 0, MOE_IDS_INT64 = 1 } moe_ids_dtype_t;
+typedef enum moe_weights_dtype { MOE_WEIGHTS_FP32 = 0, MOE_WEIGHTS_BF16 = 1 } moe_weights_dtype_t;
+typedef enum moe_activation { MOE_ACT_SILU = 0 } moe_activation_t;
+
+/* Stage mask of moe_batched_experts. */
+#define MOE_STAGE_W13 1
+#define MOE_STAGE_W2 2
+#define MOE_STAGE_ALL 3
+
+/* ------------------------------------------------------------------------ */
+/* moe_prepare_inputs                                                        */
+/*                                                                           */
+/* Defined by prepare_megamoe_inputs, _quantize_fp8_groups, _pack_bytes,     */
+/* _store_topk and _eplb_kernel_args on the page                             */
+/* "vllm.model_executor.layers.fused_moe.prepare_megamoe", and, for the      */
+/* optional dispatch, by the batched activation format of                    */
+/* BatchedHummingGroupedExperts ("...fused_moe.experts.fused_humming_moe":   */
+/* hidden_states [E, max_tokens, K] with expert_tokens_meta.expert_num_tokens).*/
+/*                                                                           */
+/* Per token t and 1x128 group g of hidden (G = K/128 groups):               */
+/*   amax = max(max|x|, 1e-4); s = amax / 448 (fp32);                        */
+/*   UE8M0: e = expfield(s) + (mantissa(s) != 0), clamped to [1, 254],       */
+/*          qs = 2^(e-127);  FP32: qs = s;                                    */
+/*   x[t, i] = e4m3_rn_satfinite(hidden[t, i] * (1 / qs)).                   */
+/* Top-k: topk_idx_out = int64(topk_ids), topk_weights_out = fp32(weights);  */
+/* padding tokens (is_padding[t] != 0) get id -1 and weight 0.               */
+/* EPLB (when logical_to_physical != NULL) maps a routed logical id l to     */
+/* logical_to_physical[l * map_stride + (t mod logical_replica_count[l])]    */
+/* and, when *should_record != 0 and t < *num_unpadded_tokens, adds 1 to     */
+/* expert_load[physical id].                                                 */
+/* Dispatch (when x_b != NULL; requires MOE_SF_UE8M0_PACKED): routes are     */
+/* placed in (token, k) order; route (t, j) with id e takes slot s, the      */
+/* number of earlier routes to e, and x_b[e, s, :] = x[t, :],                */
+/* sf_b[e, s, :] = x_sf[t, :], route_slot[t, j] = s (-1 when unrouted or     */
+/* when s >= max_tokens_per_expert, which also sets MOE_DEV_CAPACITY),       */
+/* expert_num_tokens[e] = min(#routes to e, max_tokens_per_expert).          */
+/*                                                                           */
+/* Errors: T == 0 -> MOE_OK, nothing enqueued.  K % 128 != 0 -> SHAPE.       */
+/* x_sf given iff sf_mode != NONE, else INVALID_ARGUMENT.  top_k < 1 ->       */
+/* SHAPE.  hidden / x rows must start on 16-byte boundaries (ALIGNMENT).     */
+/* Dispatch needs workspace of moe_prepare_workspace_size() bytes (WORKSPACE).*/
+/* ------------------------------------------------------------------------ */
+typedef struct moe_prepare_args {
+  int64_t num_tokens;  /* T >= 0 */
+  int64_t hidden_size; /* K, multiple of 128 */
+  int64_t top_k;       /* k >= 1 */
+
+  const void* hidden; /* bf16 [T, K], inner stride 1 */
+  int64_t hidden_stride0;
+  const void* topk_ids; /* int32 or int64 [T, k] */
+  int32_t topk_ids_dtype;
+  int64_t topk_ids_stride0, topk_ids_stride1;
+  const void* topk_weights; /* fp32 or bf16 [T, k] */
+  int32_t topk_weights_dtype;
+  int64_t topk_weights_stride0, topk_weights_stride1;
+  const uint8_t* is_padding; /* nullable; [T], nonzero = padding */
+  int64_t is_padding_stride0;
+
+  void* x; /* fp8 e4m3 [T, K] (bf16 when sf_mode == MOE_SF_NONE), inner stride 1 */
+  int64_t x_stride0;
+  void* x_sf; /* NULL iff sf_mode == MOE_SF_NONE */
+  int32_t sf_mode;
+  int64_t x_sf_stride0, x_sf_stride1;
+  int64_t* topk_idx_out; /* int64 [T, k] */
+  int64_t topk_idx_out_stride0, topk_idx_out_stride1;
+  float* topk_weights_out; /* fp32 [T, k] */
+  int64_t topk_weights_out_stride0, topk_weights_out_stride1;
+
+  /* EPLB: all NULL / 0 leaves ids unmapped. */
+  const int32_t* logical_to_physical; /* [num_logical, map_stride] */
+  int64_t num_logical, map_stride;
+  const int32_t* logical_replica_count; /* [num_logical], each >= 1 */
+  int32_t* expert_load;                 /* nullable; [num_physical] */
+  int64_t num_physical;
+  const uint8_t* should_record;       /* nullable device scalar; NULL = never record */
+  const int32_t* num_unpadded_tokens; /* nullable device scalar; NULL = T */
+
+  /* Optional dispatch into the batched layout (x_b == NULL disables it). */
+  int64_t num_experts;           /* E */
+  int64_t max_tokens_per_expert; /* M_max */
+  void* x_b;                     /* fp8 [E, M_max, K] */
+  int32_t* sf_b;                 /* int32 [E, M_max, ceil(G/4)] */
+  int32_t* expert_num_tokens;    /* int32 [E] */
+  int32_t* route_slot;           /* int32 [T, k], contiguous */
+  void* workspace;               /* moe_prepare_workspace_size() bytes */
+  size_t workspace_bytes;
+
+  uint32_t* device_status; /* nullable; MOE_DEV_* bits are OR-ed in */
+} moe_prepare_args_t;
+
+moe_status_t moe_prepare_inputs(const moe_prepare_args_t* args, void* stream);
+
+/* Bytes of workspace the dispatch of moe_prepare_inputs needs. */
+size_t moe_prepare_workspace_size(int64_t num_tokens, int64_t top_k, int64_t num_experts);
+
+/* ------------------------------------------------------------------------ */
+/* moe_batched_experts                                                       */
+/*                                                                           */
+/* Defined by BatchedHummingGroupedExperts.apply and                         */
+/* HummingExpertsBase.process_input / humming_forward / get_buffer_metas on  */
+/* the page "vllm.model_executor.layers.fused_moe.experts.fused_humming_moe" */
+/* (GROUPED_MASKED layout, block-FP8 input pre-quantised before dispatch,    */
+/* apply_router_weight_on_input false).  For each expert e and each row      */
+/* m < expert_num_tokens[e] (G = K/128, Gn = N/128):                          */
+/*   h[n]   = sum_k deq(x_b[e,m,k]) * w13[e,n,k] * w13_scale[e,n/128,k/128]  */
+/*            for n in [0, 2N); deq(x) = x * 2^(sf - 127) per 1x128 group;    */
+/*            columns [0, N) are gate, [N, 2N) up; h is rounded to bf16.      */
+/*   y[n]   = silu(h[n]) * h[N+n], silu(g) = g / (1 + exp(-g)), n < N          */
+/*   y is requantised to fp8 e4m3 in 1x128 UE8M0 groups (same recipe as      */
+/*   moe_prepare_inputs) into inter_q / inter_sf.                             */
+/*   output[e,m,c] = bf16( sum_n deq(y_q[m,n]) * w2[e,c,n] * w2_scale[e,c/128,n/128] ).*/
+/* Rows m >= expert_num_tokens[e] of output (and of inter_q) are not written.*/
+/* Accumulation is fp32; weight block scales are applied per 128-wide K      */
+/* slab in fp32.                                                              */
+/*                                                                           */
+/* Layouts: x_b [E*M_max, K] fp8, a_scale int32 [E*M_max, ceil(G/4)] packed  */
+/* UE8M0 (a_scale_mode MOE_SF_UE8M0_PACKED), w13 [E, 2N, K] fp8 K-major,     */
+/* w13_scale fp32 [E, 2N/128, G], w2 [E, K, N] fp8 N-major, w2_scale fp32     */
+/* [E, K/128, Gn], output bf16 [E, M_max, K].  All contiguous.  Base pointers*/
+/* of x_b, w13, w2, inter_q must be 16-byte aligned.                          */
+/* inter_q fp8 [E*M_max, N] and inter_sf int32 [E*M_max, ceil(Gn/4)] may be  */
+/* NULL, in which case they are carved from workspace13.  With stages ==     */
+/* MOE_STAGE_W2 the caller supplies them (the w2 stage alone).               */
+/* workspace2 holds split-K partials and tile counters.  It must be zero-    */
+/* filled once when allocated; every call leaves its counters at zero again   */
+/* (after a MOE_DEV_TIMEOUT, zero it before reuse).                           */
+/* Errors: K % 128, N % 128 -> SHAPE; activation != SILU, a_scale_mode !=    */
+/* UE8M0_PACKED -> UNSUPPORTED; short workspaces -> WORKSPACE.               */
+/* ------------------------------------------------------------------------ */
+typedef struct moe_experts_args {
+  int64_t num_experts;           /* E */
+  int64_t max_tokens_per_expert; /* M_max */
+  int64_t hidden_size;           /* K, multiple of 128 */
+  int64_t intermediate_size;     /* N, multiple of 128 */
+  int32_t activation;            /* MOE_ACT_SILU */
+  int32_t stages;                /* MOE_STAGE_* mask; 0 means MOE_STAGE_ALL */
+
+  void* output;                       /* bf16 [E, M_max, K] */
+  const void* hidden;                 /* fp8 [E*M_max, K] */
+  const void* a_scale;                /* int32 [E*M_max, ceil(G/4)] */
+  int32_t a_scale_mode;               /* MOE_SF_UE8M0_PACKED */
+  const void* w13;                    /* fp8 [E, 2N, K] */
+  const float* w13_scale;             /* [E, 2N/128, K/128] */
+  const void* w2;                     /* fp8 [E, K, N] */
+  const float* w2_scale;              /* [E, K/128, N/128] */
+  const int32_t* expert_num_tokens;   /* [E] */
+
+  void* inter_q;   /* nullable: fp8 [E*M_max, N] */
+  void* inter_sf;  /* nullable: int32 [E*M_max, ceil(Gn/4)] */
+  void* workspace13;
+  size_t workspace13_bytes;
+  void* workspace2;
+  size_t workspace2_bytes;
+  int64_t valid_shape_m; /* tuning hint: expected routed rows (T * k); <= 0 = E * M_max */
+  void* gate_up_dump;    /* nullable: bf16 [E*M_max, 2N] copy of h (debug/parity) */
+  uint32_t* device_status;
+} moe_experts_args_t;
+
+moe_status_t moe_batched_experts(const moe_experts_args_t* args, void* stream);
+
+/* Workspace bytes: which = 13 (workspace13: inter_q + inter_sf) or 2
+ * (workspace2: split-K partials + tile counters for this valid_shape_m). */
+size_t moe_batched_experts_workspace_size(int64_t num_experts, int64_t max_tokens_per_expert,
+                                          int64_t hidden_size, int64_t intermediate_size,
+                                          int64_t valid_shape_m, int which);
+
+/* ------------------------------------------------------------------------ */
+/* moe_topk_reduce                                                           */
+/*                                                                           */
+/* Defined by the finalize step of BatchedHummingGroupedExperts              */
+/* (finalize_weight_and_reduce_impl -> TopKWeightAndReduceDelegate) and the  */
+/* weighted top-k sum of moe_fused_mul_sum in HummingIndexedExperts.apply     */
+/* ("...fused_moe.experts.fused_humming_moe"):                               */
+/*   out[t, c] = bf16( sum_{j < k, idx[t,j] >= 0, slot[t,j] >= 0}            */
+/*                     w[t,j] * expert_out[idx[t,j], slot[t,j], c] )          */
+/* summed in fp32 in ascending j; tokens without a placed route get 0.       */
+/* expert_out bf16 [E, M_max, K]; topk_idx int64 [T, k]; route_slot int32    */
+/* [T, k]; topk_weights fp32 [T, k]; out bf16 [T, K]; all contiguous; the    */
+/* expert_out and out base pointers 16-byte aligned; K % 8 == 0.             */
+/* ------------------------------------------------------------------------ */
+moe_status_t moe_topk_reduce(const void* expert_out, int64_t num_experts,
+                             int64_t max_tokens_per_expert, int64_t hidden_size,
+                             const int64_t* topk_idx, const int32_t* route_slot,
+                             const float* topk_weights, int64_t num_tokens, int64_t top_k,
+                             void* out, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Utilities                                                                 */
+/* ------------------------------------------------------------------------ */
+int moe_abi_version(void);
+/* Message of the last host-side error on this thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_PREP_H */

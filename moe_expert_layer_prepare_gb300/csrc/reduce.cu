@@ -1,0 +1,86 @@
+// Top-k weighted reduce back to token order.
+//
+// Follows the finalize step of BatchedHummingGroupedExperts
+// (TopKWeightAndReduceDelegate) and the weighted top-k sum of
+// moe_fused_mul_sum in HummingIndexedExperts.apply
+// ("vllm.model_executor.layers.fused_moe.experts.fused_humming_moe").
+//
+// One warp per (token, 256-column chunk); each lane owns 8 columns (16 bytes).
+// For each j in ascending order the routed expert row is read with a
+// streaming 16-byte load, weighted in fp32 and accumulated; one bf16 rounding
+// at the end.  HBM-bound: each routed row is read once, each output row
+// written once.
+#include "common.cuh"
+
+namespace moe {
+
+struct ReduceParams {
+  const uint16_t* expert_out;  // bf16 [E*M_max, K]
+  int64_t E, M_max, K;
+  const int64_t* idx;    // [T, k]
+  const int32_t* slot;   // [T, k]
+  const float* w;        // [T, k]
+  int64_t T, top_k;
+  uint16_t* out;         // bf16 [T, K]
+};
+
+__global__ void __launch_bounds__(256) topk_reduce_kernel(ReduceParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t chunks = (p.K + 255) / 256;
+  const int64_t tasks = p.T * chunks;
+  for (int64_t task = gwarp; task < tasks; task += nwarps) {
+    const int64_t t = task / chunks;
+    const int64_t c0 = (task - t * chunks) * 256 + lane * 8;
+    const bool active = c0 < p.K;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int64_t j = 0; j < p.top_k; ++j) {
+      const int64_t e = p.idx[t * p.top_k + j];
+      const int32_t s = p.slot[t * p.top_k + j];
+      if (e < 0 || s < 0 || e >= p.E || s >= p.M_max) continue;
+      const float wt = p.w[t * p.top_k + j];
+      if (active) {
+        const uint4 v = ld_stream_v4(p.expert_out + (e * p.M_max + s) * p.K + c0);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wt, bf16_bits_to_f32(u[i] & 0xFFFFu), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wt, bf16_bits_to_f32(u[i] >> 16), acc[2 * i + 1]);
+        }
+      }
+    }
+    if (active) {
+      uint4 o;
+      o.x = f32_to_bf16_bits(acc[0]) | (f32_to_bf16_bits(acc[1]) << 16);
+      o.y = f32_to_bf16_bits(acc[2]) | (f32_to_bf16_bits(acc[3]) << 16);
+      o.z = f32_to_bf16_bits(acc[4]) | (f32_to_bf16_bits(acc[5]) << 16);
+      o.w = f32_to_bf16_bits(acc[6]) | (f32_to_bf16_bits(acc[7]) << 16);
+      st_v4(p.out + t * p.K + c0, o);
+    }
+  }
+}
+
+}  // namespace moe
+
+namespace moe_host {
+
+moe_status_t launch_topk_reduce(const void* expert_out, int64_t E, int64_t M_max, int64_t K,
+                                const int64_t* idx, const int32_t* slot, const float* w,
+                                int64_t T, int64_t top_k, void* out, cudaStream_t s) {
+  moe::ReduceParams p{static_cast<const uint16_t*>(expert_out), E, M_max, K, idx, slot, w, T,
+                      top_k, static_cast<uint16_t*>(out)};
+  const int64_t tasks = T * ((K + 255) / 256);
+  int64_t blocks = (tasks * 32 + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  moe::topk_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "reduce launch: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+}  // namespace moe_host

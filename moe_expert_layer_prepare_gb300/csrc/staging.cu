@@ -1,0 +1,422 @@
+// Input staging: bf16 -> fp8 e4m3 with 1x128 UE8M0 (or fp32) group scales,
+// top-k repack with EPLB replica mapping, and the dispatch into the batched
+// [E, M_max, K] layout.
+//
+// Follows prepare_megamoe_inputs / _quantize_fp8_groups / _pack_bytes /
+// _store_topk / _eplb_kernel_args ("vllm.model_executor.layers.fused_moe.
+// prepare_megamoe") and the BatchedExperts activation format of
+// BatchedHummingGroupedExperts ("...fused_moe.experts.fused_humming_moe").
+//
+// Kernels
+//   route_kernel : one thread per route (t, j), 1024 routes per block.  Repack
+//                  + EPLB + per-block expert histogram + the stable rank of the
+//                  route among the block's routes to the same expert.  The last
+//                  block to finish turns the histograms into per-block
+//                  exclusive offsets (column scan over blocks) and writes
+//                  expert_num_tokens.
+//   quant_kernel : one warp per (token, 4 groups = 512 elements): 16-byte
+//                  loads, warp-shuffle amax over the 8 lanes of a group, packed
+//                  fp8 stores, one packed exponent word per task; optionally
+//                  the same bytes are stored into each routed slot of x_b.
+//                  Without dispatch the repack is folded into this kernel.
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct StageParams {
+  int64_t T, K, top_k, G, W;  // W = ceil(G/4) packed words per row
+  const uint16_t* hidden;
+  int64_t hs0;
+  const void* ids;
+  int64_t is0, is1;
+  const void* wts;
+  int64_t ws0, ws1;
+  const uint8_t* pad;
+  int64_t ps0;
+  uint8_t* x;
+  int64_t xs0;
+  void* x_sf;
+  int64_t sfs0, sfs1;
+  int64_t* ids_out;
+  int64_t ios0, ios1;
+  float* w_out;
+  int64_t wos0, wos1;
+  const int32_t* l2p;
+  int64_t num_logical, map_stride;
+  const int32_t* rep_count;
+  int32_t* load;
+  int64_t num_physical;
+  const uint8_t* record;
+  const int32_t* num_unpadded;
+  // dispatch
+  int64_t E, M_max;
+  uint8_t* x_b;
+  int32_t* sf_b;
+  int32_t* expert_num_tokens;
+  int32_t* route_slot;
+  int32_t* hist;        // [B, E] -> exclusive offsets after the scan
+  int32_t* local_rank;  // [T*k]
+  uint32_t* done;       // block completion counter (zeroed by the host)
+  int64_t num_route_blocks;
+  uint32_t* status;
+};
+
+// Repack one route (t, j): int64 id (-1 for padding), fp32 weight, EPLB map and
+// load record.  Returns the id written.
+template <typename IdT, typename WT>
+__device__ __forceinline__ int64_t repack_route(const StageParams& p, int64_t t, int64_t j,
+                                                bool record_on, int64_t unpadded) {
+  bool is_pad = p.pad ? (p.pad[t * p.ps0] != 0) : false;
+  int64_t id = (int64_t)(reinterpret_cast<const IdT*>(p.ids)[t * p.is0 + j * p.is1]);
+  float w;
+  if constexpr (sizeof(WT) == 4) {
+    w = reinterpret_cast<const float*>(p.wts)[t * p.ws0 + j * p.ws1];
+  } else {
+    w = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.wts)[t * p.ws0 + j * p.ws1]);
+  }
+  if (is_pad) {
+    id = -1;
+    w = 0.0f;
+  }
+  if (p.l2p != nullptr && id >= 0) {
+    if (id >= p.num_logical) {
+      set_status(p.status, MOE_DEV_BAD_EXPERT);
+      id = -1;
+    } else {
+      int32_t reps = p.rep_count[id];
+      if (reps < 1) {
+        set_status(p.status, MOE_DEV_BAD_EXPERT);
+        id = -1;
+      } else {
+        int64_t phys = p.l2p[id * p.map_stride + (t % reps)];
+        if (phys < 0 || (p.load != nullptr && phys >= p.num_physical)) {
+          set_status(p.status, MOE_DEV_BAD_EXPERT);
+          id = -1;
+        } else {
+          id = phys;
+          if (p.load != nullptr && record_on && t < unpadded) atomicAdd(&p.load[phys], 1);
+        }
+      }
+    }
+  }
+  p.ids_out[t * p.ios0 + j * p.ios1] = id;
+  p.w_out[t * p.wos0 + j * p.wos1] = w;
+  return id;
+}
+
+__device__ __forceinline__ void record_flags(const StageParams& p, bool& record_on,
+                                             int64_t& unpadded) {
+  record_on = p.record != nullptr && (*p.record != 0);
+  unpadded = p.num_unpadded != nullptr ? (int64_t)(*p.num_unpadded) : p.T;
+}
+
+// ---------------------------------------------------------------------------
+// route_kernel: repack + EPLB + stable within-block ranks + histogram scan.
+// blockDim = 1024; dynamic smem = 32 * E uint16 warp counts.
+// ---------------------------------------------------------------------------
+template <typename IdT, typename WT>
+__global__ void __launch_bounds__(1024) route_kernel(StageParams p) {
+  extern __shared__ uint16_t warp_cnt[];  // [32][E]
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t R = p.T * p.top_k;
+  const int64_t r = (int64_t)blockIdx.x * 1024 + tid;
+  const int E = (int)p.E;
+
+  for (int i = tid; i < 32 * E; i += 1024) warp_cnt[i] = 0;
+
+  bool record_on;
+  int64_t unpadded;
+  record_flags(p, record_on, unpadded);
+
+  int e = -1;
+  if (r < R) {
+    int64_t t = r / p.top_k, j = r % p.top_k;
+    int64_t id = repack_route<IdT, WT>(p, t, j, record_on, unpadded);
+    if (id >= E) {
+      set_status(p.status, MOE_DEV_BAD_EXPERT);
+      id = -1;
+    }
+    e = (int)id;
+  }
+  __syncthreads();  // warp_cnt zeroed
+
+  // Stable rank among this warp's routes to the same expert.
+  const uint32_t same = __match_any_sync(0xFFFFFFFFu, e);
+  const int rank_in_warp = __popc(same & lanemask_lt());
+  if (e >= 0 && rank_in_warp == 0) warp_cnt[warp * E + e] = (uint16_t)__popc(same);
+  __syncthreads();
+  if (e >= 0) {
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_cnt[w * E + e];
+    p.local_rank[r] = base + rank_in_warp;
+  }
+  // Block histogram row.
+  for (int ex = tid; ex < E; ex += 1024) {
+    int tot = 0;
+#pragma unroll 8
+    for (int w = 0; w < 32; ++w) tot += warp_cnt[w * E + ex];
+    p.hist[(int64_t)blockIdx.x * E + ex] = tot;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(p.done, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // Last block: column-wise exclusive scan of hist over blocks.
+  const int64_t B = p.num_route_blocks;
+  for (int ex = tid; ex < E; ex += 1024) {
+    int run = 0;
+    for (int64_t b = 0; b < B; ++b) {
+      int v = __ldcg(&p.hist[b * E + ex]);
+      p.hist[b * E + ex] = run;
+      run += v;
+    }
+    if (run > p.M_max) set_status(p.status, MOE_DEV_CAPACITY);
+    p.expert_num_tokens[ex] = (int32_t)min((int64_t)run, p.M_max);
+  }
+  if (tid == 0) *p.done = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// quant_kernel: one warp per (token t, word w) task = groups 4w .. 4w+3.
+// Lane l covers 16 elements of group 4w + l/8.
+// ---------------------------------------------------------------------------
+template <int SF_MODE, bool REPACK, bool DISPATCH, typename IdT, typename WT>
+__global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+
+  if constexpr (REPACK) {
+    bool record_on;
+    int64_t unpadded;
+    record_flags(p, record_on, unpadded);
+    const int64_t R = p.T * p.top_k;
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R;
+         r += (int64_t)gridDim.x * blockDim.x)
+      repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
+  }
+
+  const int grp = lane >> 3;
+  const int sub = lane & 7;
+  const int64_t tasks = p.T * p.W;
+  for (int64_t task = gwarp; task < tasks; task += nwarps) {
+    const int64_t t = task / p.W;
+    const int64_t w = task - t * p.W;
+    const int64_t g = 4 * w + grp;
+    const bool active = g < p.G;
+    const int64_t col = g * kGroup + sub * 16;
+    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+    if (active) {
+      const uint16_t* src = p.hidden + t * p.hs0 + col;
+      v0 = ld_stream_v4(src);
+      v1 = ld_stream_v4(src + 8);
+    }
+    if constexpr (SF_MODE == MOE_SF_NONE) {
+      if (active) {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.x) + t * p.xs0 + col;
+        st_v4(dst, v0);
+        st_v4(dst + 8, v1);
+      }
+      continue;
+    } else {
+      float f[16];
+      const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
+        f[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      uint32_t code;
+      float inv;
+      if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
+        code = ue8m0_exponent(amax);
+        inv = __frcp_rn(__uint_as_float(code << 23));
+      } else {
+        float s = __fdiv_rn(fmaxf(amax, 1.0e-4f), 448.0f);
+        code = __float_as_uint(s);
+        inv = __frcp_rn(s);
+      }
+      uint4 q;
+      q.x = pack4_e4m3(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                       __fmul_rn(f[3], inv));
+      q.y = pack4_e4m3(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),
+                       __fmul_rn(f[7], inv));
+      q.z = pack4_e4m3(__fmul_rn(f[8], inv), __fmul_rn(f[9], inv), __fmul_rn(f[10], inv),
+                       __fmul_rn(f[11], inv));
+      q.w = pack4_e4m3(__fmul_rn(f[12], inv), __fmul_rn(f[13], inv), __fmul_rn(f[14], inv),
+                       __fmul_rn(f[15], inv));
+      if (active) st_v4(p.x + t * p.xs0 + col, q);
+
+      uint32_t word = 0;
+      if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
+        const uint32_t mine = active ? code : 0u;
+        const uint32_t e0 = __shfl_sync(0xFFFFFFFFu, mine, 0);
+        const uint32_t e1 = __shfl_sync(0xFFFFFFFFu, mine, 8);
+        const uint32_t e2 = __shfl_sync(0xFFFFFFFFu, mine, 16);
+        const uint32_t e3 = __shfl_sync(0xFFFFFFFFu, mine, 24);
+        word = e0 | (e1 << 8) | (e2 << 16) | (e3 << 24);
+        if (lane == 0)
+          reinterpret_cast<uint32_t*>(p.x_sf)[t * p.sfs0 + w * p.sfs1] = word;
+      } else {
+        if (active && sub == 0)
+          reinterpret_cast<float*>(p.x_sf)[t * p.sfs0 + g * p.sfs1] = __uint_as_float(code);
+      }
+
+      if constexpr (DISPATCH) {
+        const int64_t K = p.K;
+        for (int64_t j = 0; j < p.top_k; ++j) {
+          const int64_t r = t * p.top_k + j;
+          const int64_t e = p.ids_out[t * p.ios0 + j * p.ios1];
+          int64_t slot = -1;
+          if (e >= 0 && e < p.E) {
+            slot = (int64_t)__ldcg(&p.hist[(r >> 10) * p.E + e]) + p.local_rank[r];
+            if (slot >= p.M_max) slot = -1;
+          }
+          if (slot >= 0) {
+            const int64_t row = e * p.M_max + slot;
+            if (active) st_v4(p.x_b + row * K + col, q);
+            if (lane == 0) p.sf_b[row * p.W + w] = (int32_t)word;
+          }
+          if (w == 0 && lane == 0) p.route_slot[r] = (int32_t)slot;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+namespace moe_host {
+
+using moe::StageParams;
+
+size_t prepare_workspace_size(int64_t T, int64_t k, int64_t E) {
+  const int64_t R = T * k;
+  const int64_t B = (R + 1023) / 1024;
+  size_t bytes = 256;                                   // completion counter
+  bytes += (size_t)((B * E * 4 + 255) / 256) * 256;     // hist
+  bytes += (size_t)((R * 4 + 255) / 256) * 256;         // local ranks
+  return bytes;
+}
+
+template <typename IdT, typename WT>
+static moe_status_t launch_typed(StageParams& p, bool dispatch, int sf_mode, cudaStream_t s) {
+  const int sms = num_sms();
+  const int64_t tasks = p.T * p.W;
+  const int threads = 256;
+  int64_t blocks = (tasks * 32 + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * 8;  // 8 resident blocks of 256 threads per SM
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (dispatch) {
+    const int64_t R = p.T * p.top_k;
+    const int64_t B = (R + 1023) / 1024;
+    p.num_route_blocks = B;
+    const size_t smem = (size_t)32 * p.E * sizeof(uint16_t);
+    auto rk = moe::route_kernel<IdT, WT>;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+      if (e != cudaSuccess)
+        return set_error(MOE_ERR_CUDA, "route_kernel smem attribute: %s", cudaGetErrorString(e));
+    }
+    cudaError_t e = cudaMemsetAsync(p.done, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    rk<<<(unsigned)B, 1024, smem, s>>>(p);
+    moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT>
+        <<<(unsigned)blocks, threads, 0, s>>>(p);
+  } else {
+    switch (sf_mode) {
+      case MOE_SF_NONE:
+        moe::quant_kernel<MOE_SF_NONE, true, false, IdT, WT><<<(unsigned)blocks, threads, 0, s>>>(p);
+        break;
+      case MOE_SF_UE8M0_PACKED:
+        moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT>
+            <<<(unsigned)blocks, threads, 0, s>>>(p);
+        break;
+      default:
+        moe::quant_kernel<MOE_SF_FP32, true, false, IdT, WT><<<(unsigned)blocks, threads, 0, s>>>(p);
+        break;
+    }
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "staging launch: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s) {
+  StageParams p{};
+  p.T = a->num_tokens;
+  p.K = a->hidden_size;
+  p.top_k = a->top_k;
+  p.G = a->hidden_size / 128;
+  p.W = (p.G + 3) / 4;
+  p.hidden = static_cast<const uint16_t*>(a->hidden);
+  p.hs0 = a->hidden_stride0;
+  p.ids = a->topk_ids;
+  p.is0 = a->topk_ids_stride0;
+  p.is1 = a->topk_ids_stride1;
+  p.wts = a->topk_weights;
+  p.ws0 = a->topk_weights_stride0;
+  p.ws1 = a->topk_weights_stride1;
+  p.pad = a->is_padding;
+  p.ps0 = a->is_padding_stride0;
+  p.x = static_cast<uint8_t*>(a->x);
+  p.xs0 = a->x_stride0;
+  p.x_sf = a->x_sf;
+  p.sfs0 = a->x_sf_stride0;
+  p.sfs1 = a->x_sf_stride1;
+  p.ids_out = a->topk_idx_out;
+  p.ios0 = a->topk_idx_out_stride0;
+  p.ios1 = a->topk_idx_out_stride1;
+  p.w_out = a->topk_weights_out;
+  p.wos0 = a->topk_weights_out_stride0;
+  p.wos1 = a->topk_weights_out_stride1;
+  p.l2p = a->logical_to_physical;
+  p.num_logical = a->num_logical;
+  p.map_stride = a->map_stride;
+  p.rep_count = a->logical_replica_count;
+  p.load = a->expert_load;
+  p.num_physical = a->num_physical;
+  p.record = a->should_record;
+  p.num_unpadded = a->num_unpadded_tokens;
+  p.status = a->device_status;
+  const bool dispatch = a->x_b != nullptr;
+  if (dispatch) {
+    p.E = a->num_experts;
+    p.M_max = a->max_tokens_per_expert;
+    p.x_b = static_cast<uint8_t*>(a->x_b);
+    p.sf_b = a->sf_b;
+    p.expert_num_tokens = a->expert_num_tokens;
+    p.route_slot = a->route_slot;
+    const int64_t R = p.T * p.top_k;
+    const int64_t B = (R + 1023) / 1024;
+    char* ws = static_cast<char*>(a->workspace);
+    p.done = reinterpret_cast<uint32_t*>(ws);
+    p.hist = reinterpret_cast<int32_t*>(ws + 256);
+    p.local_rank = reinterpret_cast<int32_t*>(ws + 256 + ((B * p.E * 4 + 255) / 256) * 256);
+  }
+  const bool ids64 = a->topk_ids_dtype == MOE_IDS_INT64;
+  const bool wbf16 = a->topk_weights_dtype == MOE_WEIGHTS_BF16;
+  if (ids64)
+    return wbf16 ? launch_typed<int64_t, uint16_t>(p, dispatch, a->sf_mode, s)
+                 : launch_typed<int64_t, float>(p, dispatch, a->sf_mode, s);
+  return wbf16 ? launch_typed<int32_t, uint16_t>(p, dispatch, a->sf_mode, s)
+               : launch_typed<int32_t, float>(p, dispatch, a->sf_mode, s);
+}
+
+}  // namespace moe_host

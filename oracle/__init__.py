@@ -74,6 +74,8 @@ def _load():
         lib.orc_dispatch.argtypes = [i64, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, vp]
         lib.orc_w13_rows.restype = None
         lib.orc_w13_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_silu_requant_rows.restype = None
+        lib.orc_silu_requant_rows.argtypes = [i64, vp, i64, vp, vp, vp]
         lib.orc_w2_rows.restype = None
         lib.orc_w2_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp]
         lib.orc_topk_reduce.restype = None
@@ -209,6 +211,18 @@ def w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h=False):
     return h, y_q, y_sf
 
 
+def silu_requant_rows(rows, N, h_bits):
+    """SiLU-and-mul + 1x128 UE8M0 requant of given bf16 h rows [R, 2N]."""
+    lib = _load()
+    rows = _c(rows, np.int64)
+    h = _c(h_bits, np.uint16)
+    R = h.shape[0]
+    y_q = np.zeros((R, N), np.uint8)
+    y_sf = np.zeros((R, (N // 128 + 3) // 4), np.int32)
+    lib.orc_silu_requant_rows(rows.size, _p(rows), N, _p(h), _p(y_q), _p(y_sf))
+    return y_q, y_sf
+
+
 def w2_rows(rows, M_max, K, N, y_q, y_sf, w2, w2_s):
     """w2 GEMM for the given global rows; returns bf16 bits [E*M_max, K]."""
     lib = _load()
@@ -253,3 +267,70 @@ def forward(hidden_bf16_bits, topk_ids, topk_weights, w13, w13_s, w2, w2_s, E, M
     out = topk_reduce(out_b, st["ids"], d["route_slot"], st["weights"], M_max)
     return dict(staging=st, dispatch=d, rows=rows, h=h, y_q=y_q, y_sf=y_sf, out_b=out_b,
                 out=out)
+
+
+def sampled_forward(hidden_bits, topk_ids, topk_weights, is_padding, E, M_max, N, tokens,
+                    weights_of, want_h=False, timings=None):
+    """S1-S8 for a sample of tokens of a full-size workload.
+
+    Routing and dispatch run over every token (so the slots are the full
+    problem's); quantisation and the expert GEMMs run only for the sampled
+    tokens' routes, on a compact copy of the experts they touch, fetched with
+    ``weights_of(experts) -> (w13, w13_s, w2, w2_s)``.  ``timings`` (a dict)
+    receives the wall time of the arithmetic and the FLOPs it covered.
+    """
+    import time
+    T, K = hidden_bits.shape
+    k = topk_ids.shape[1]
+    tokens = np.asarray(tokens, np.int64)
+    st_all = prepare_inputs(np.zeros((T, 128), np.uint16), topk_ids, topk_weights,
+                            is_padding=is_padding)
+    d = dispatch(st_all["ids"], np.zeros((T, 128), np.uint8), np.zeros((T, 1), np.int32),
+                 E, M_max, copy_rows=False)
+    routes = []
+    for i, t in enumerate(tokens):
+        for j in range(k):
+            e, s = int(st_all["ids"][t, j]), int(d["route_slot"][t, j])
+            if e >= 0 and s >= 0:
+                routes.append((i, j, e, s))
+    experts = sorted({r[2] for r in routes})
+    w13, w13_s, w2, w2_s = weights_of(experts) if experts else (None,) * 4
+    t0 = time.perf_counter()
+    st = prepare_inputs(hidden_bits[tokens], topk_ids[tokens], topk_weights[tokens],
+                        is_padding=None if is_padding is None else is_padding[tokens])
+    cidx = {e: n for n, e in enumerate(experts)}
+    counts = {}
+    for r in routes:
+        counts[r[2]] = counts.get(r[2], 0) + 1
+    Mc = max([1] + list(counts.values()))
+    W = st["x_sf"].shape[1]
+    nE = max(len(experts), 1)
+    x_b = np.zeros((nE * Mc, K), np.uint8)
+    sf_b = np.zeros((nE * Mc, W), np.int32)
+    cids = np.full((len(tokens), k), -1, np.int64)
+    cslot = np.full((len(tokens), k), -1, np.int32)
+    crow_of = {}
+    per = {}
+    for (i, j, e, s) in routes:
+        n = per.get(e, 0)
+        per[e] = n + 1
+        r = cidx[e] * Mc + n
+        x_b[r] = st["x"][i]
+        sf_b[r] = st["x_sf"][i]
+        cids[i, j] = cidx[e]
+        cslot[i, j] = n
+        crow_of[(i, j)] = r
+    rows = np.array(sorted(crow_of.values()), np.int64)
+    if rows.size:
+        h, y_q, y_sf = w13_rows(rows, Mc, K, N, x_b, sf_b, w13, w13_s, want_h=want_h)
+        out_b = w2_rows(rows, Mc, K, N, y_q, y_sf, w2, w2_s)
+    else:
+        h = y_q = y_sf = None
+        out_b = np.zeros((nE * Mc, K), np.uint16)
+    out = topk_reduce(out_b, cids, cslot, st["weights"], Mc)
+    if timings is not None:
+        timings["seconds"] = time.perf_counter() - t0
+        timings["flops"] = 6.0 * N * K * len(routes)
+        timings["routes"] = len(routes)
+    return dict(out=out, routes=routes, crow_of=crow_of, h=h, y_q=y_q, y_sf=y_sf, out_b=out_b,
+                dispatch=d, ids=st_all["ids"], staging=st)

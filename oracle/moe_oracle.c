@@ -261,6 +261,26 @@ static double a_scale_of(const int32_t* sf_words, int64_t W, int64_t row, int64_
   return ldexp(1.0, e - 127);
 }
 
+/* SiLU-and-mul of one row of bf16 h (gate [0,N), up [N,2N)) and the 1x128
+ * UE8M0 requant of y along N (HummingExpertsBase.process_input with an
+ * activation; the same group recipe as _quantize_fp8_groups). */
+static void silu_requant_row(const double* hb, int64_t N, uint8_t* yq_row, uint32_t* ysf_row) {
+  const int64_t Gn = N / 128, Wy = (Gn + 3) / 4;
+  float* y = (float*)malloc(sizeof(float) * (size_t)N);
+  for (int64_t n = 0; n < N; ++n) {
+    double g = hb[n], u = hb[N + n];
+    double silu = g / (1.0 + exp(-g));
+    y[n] = (float)(silu * u);
+  }
+  for (int64_t w = 0; w < Wy; ++w) ysf_row[w] = 0;
+  for (int64_t g = 0; g < Gn; ++g) {
+    uint32_t code;
+    quantize_group_f32(y + g * 128, 128, 1, yq_row + g * 128, &code, NULL);
+    ysf_row[g / 4] |= (code & 0xFFu) << (8 * (g % 4));
+  }
+  free(y);
+}
+
 void orc_w13_rows(int64_t n_rows, const int64_t* rows, int64_t M_max, int64_t K, int64_t N,
                   const uint8_t* x_b, const int32_t* a_sf, const uint8_t* w13,
                   const float* w13_s, uint16_t* h_out, uint8_t* y_q, int32_t* y_sf) {
@@ -273,7 +293,6 @@ void orc_w13_rows(int64_t n_rows, const int64_t* rows, int64_t M_max, int64_t K,
     const int64_t e = r / M_max;
     double* a = (double*)malloc(sizeof(double) * (size_t)K);
     double* hb = (double*)malloc(sizeof(double) * (size_t)twoN);
-    float* y = (float*)malloc(sizeof(float) * (size_t)N);
     for (int64_t k = 0; k < K; ++k)
       a[k] = (double)orc_e4m3_decode(x_b[r * K + k]) * a_scale_of(a_sf, Wa, r, k / 128);
     for (int64_t j = 0; j < twoN; ++j) {
@@ -286,20 +305,23 @@ void orc_w13_rows(int64_t n_rows, const int64_t* rows, int64_t M_max, int64_t K,
       if (h_out) h_out[r * twoN + j] = hbits;
       hb[j] = (double)bf16_to_f32(hbits);
     }
-    for (int64_t n = 0; n < N; ++n) {
-      double g = hb[n], u = hb[N + n];
-      double silu = g / (1.0 + exp(-g));
-      y[n] = (float)(silu * u);
-    }
-    for (int64_t w = 0; w < Wy; ++w) y_sf[r * Wy + w] = 0;
-    for (int64_t g = 0; g < Gn; ++g) {
-      uint32_t code;
-      quantize_group_f32(y + g * 128, 128, 1, y_q + r * N + g * 128, &code, NULL);
-      ((uint32_t*)y_sf)[r * Wy + g / 4] |= (code & 0xFFu) << (8 * (g % 4));
-    }
+    silu_requant_row(hb, N, y_q + r * N, (uint32_t*)y_sf + r * Wy);
     free(a);
     free(hb);
-    free(y);
+  }
+}
+
+/* S7a second half alone: SiLU-and-mul + requant of given bf16 h rows. */
+void orc_silu_requant_rows(int64_t n_rows, const int64_t* rows, int64_t N, const uint16_t* h,
+                           uint8_t* y_q, int32_t* y_sf) {
+  const int64_t Wy = (N / 128 + 3) / 4;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n_rows; ++i) {
+    const int64_t r = rows[i];
+    double* hb = (double*)malloc(sizeof(double) * (size_t)(2 * N));
+    for (int64_t j = 0; j < 2 * N; ++j) hb[j] = (double)bf16_to_f32(h[r * 2 * N + j]);
+    silu_requant_row(hb, N, y_q + r * N, (uint32_t*)y_sf + r * Wy);
+    free(hb);
   }
 }
 

@@ -1,0 +1,182 @@
+"""GPU parity of moe_batched_experts (w13 GEMM + SiLU-and-mul requant + w2
+GEMM) and of the whole path against the oracle.
+
+* h (gate_up_output, bf16) and the final outputs: FP tolerance (normwise
+  relative error <= 1e-2, elementwise |d| <= 3e-2 (|ref| + rms(ref))).
+* requantised w2 input: the oracle's SiLU-and-mul + requant applied to the
+  GPU's own bf16 h; codes equal except where the different exp moves a value
+  across a rounding boundary (one step).
+* w2 stage alone, fed the oracle's y_q / y_sf: FP tolerance.
+* rows >= expert_num_tokens of the output stay untouched (sentinels).
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_expert_layer_prepare_gb300 import binding as B
+from moe_expert_layer_prepare_gb300 import synthetic as syn
+from tests._util import (assert_codes_close, assert_fp_close, bf16_bits, bf16_vals,
+                         need_cuda, oracle_sampled_forward, unpack_exponents)
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = -1  # 0xFFFF bf16 pattern (a NaN) in every output row
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    need_cuda()
+    from moe_expert_layer_prepare_gb300 import build
+    build.build()
+    B.load()
+    return torch.device("cuda")
+
+
+def _layer(wl, dev, valid_shape_m=None):
+    c = wl["cfg"]
+    to = lambda t: t.to(dev)  # noqa: E731
+    return B.MoeLayer(c["T"], c["K"], c["N"], c["E"], c["top_k"], c["M_max"], to(wl["w13"]),
+                      to(wl["w13_s"]), to(wl["w2"]), to(wl["w2_s"]), device=dev,
+                      valid_shape_m=valid_shape_m)
+
+
+def _run_layer(layer, wl, dev, dump=False):
+    c = wl["cfg"]
+    layer.out_b.view(torch.int16).fill_(SENTINEL)
+    h = None
+    if dump:
+        h = torch.zeros((c["E"] * c["M_max"], 2 * c["N"]), dtype=torch.bfloat16, device=dev)
+    layer.prepare(wl["hidden"].to(dev), wl["topk_ids"].to(dev), wl["topk_weights"].to(dev),
+                  wl["is_padding"].to(dev))
+    layer.experts(gate_up_dump=h)
+    layer.reduce()
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    return h
+
+
+def _custom_workload(T, K, N, E, k, M_max, seed, zipf=None):
+    wl = dict(cfg=dict(T=T, K=K, N=N, E=E, top_k=k, M_max=M_max))
+    wl["hidden"] = syn.make_hidden(T, K, seed)
+    wl["topk_ids"], wl["topk_weights"], wl["is_padding"] = syn.make_routing(
+        T, E, k, seed + 1, zipf_s=zipf, padding_frac=0.03)
+    wl["w13"], wl["w13_s"] = syn.make_block_fp8_weights(E, 2 * N, K, seed + 2)
+    wl["w2"], wl["w2_s"] = syn.make_block_fp8_weights(E, K, N, seed + 3)
+    return wl
+
+
+def _full_check(orc, wl, layer, h_gpu):
+    """Oracle on every token; compare dispatch, h, requant, w2 alone, output."""
+    c = wl["cfg"]
+    T, K, N, E, M = c["T"], c["K"], c["N"], c["E"], c["M_max"]
+    table = orc.e4m3_decode_table()
+    args = [wl[n].numpy() for n in ("w13", "w13_s", "w2", "w2_s")]
+    ref = orc.forward(bf16_bits(wl["hidden"]), wl["topk_ids"].numpy(),
+                      wl["topk_weights"].numpy(), *args, E, M, N,
+                      is_padding=wl["is_padding"].numpy(), want_h=True)
+    n = ref["dispatch"]["expert_num_tokens"]
+    assert np.array_equal(layer.expert_num_tokens.cpu().numpy(), n)
+    assert np.array_equal(layer.route_slot.cpu().numpy(), ref["dispatch"]["route_slot"])
+    rows = ref["rows"]
+    # h: bf16 gate_up_output
+    hg = bf16_vals(bf16_bits(h_gpu))[rows]
+    hr = bf16_vals(ref["h"])[rows]
+    assert_fp_close(hg, hr, "gate_up_output")
+    # requant of the GPU's own h
+    q_gpu, sf_gpu = layer.inter()
+    yq_ref, ysf_ref = orc.silu_requant_rows(rows, N, bf16_bits(h_gpu))
+    Gn = N // 128
+    eg = unpack_exponents(sf_gpu.cpu().numpy()[rows], Gn)
+    er = unpack_exponents(ysf_ref[rows], Gn)
+    assert np.mean(eg == er) > 0.999
+    assert np.all(np.abs(eg.astype(int) - er.astype(int)) <= 1)
+    assert_codes_close(q_gpu.cpu().numpy()[rows], yq_ref[rows], table, "requant codes")
+    # output rows and sentinels
+    ob = bf16_vals(bf16_bits(layer.out_b).reshape(E * M, K))
+    assert_fp_close(ob[rows], bf16_vals(ref["out_b"])[rows], "down_output")
+    raw = bf16_bits(layer.out_b).reshape(E, M, K)
+    for e in range(E):
+        assert np.all(raw[e, n[e]:] == 0xFFFF), f"expert {e}: rows past {n[e]} were written"
+    assert_fp_close(bf16_vals(bf16_bits(layer.out)), bf16_vals(ref["out"]), "output")
+    return ref
+
+
+def _w2_alone(orc, wl, layer, ref, dev):
+    c = wl["cfg"]
+    E, M, K, N = c["E"], c["M_max"], c["K"], c["N"]
+    out_b = torch.empty((E, M, K), dtype=torch.bfloat16, device=dev)
+    out_b.view(torch.int16).fill_(SENTINEL)
+    inter_q = torch.from_numpy(ref["y_q"]).to(dev)
+    inter_sf = torch.from_numpy(ref["y_sf"]).to(dev)
+    B.moe_batched_experts(out_b, None, None, layer.w13, layer.w13_s, layer.w2, layer.w2_s,
+                          layer.expert_num_tokens, None, layer.ws2,
+                          valid_shape_m=layer.valid_shape_m, inter_q=inter_q, inter_sf=inter_sf,
+                          stages=B.MOE_STAGE_W2)
+    torch.cuda.synchronize()
+    rows = ref["rows"]
+    got = bf16_vals(bf16_bits(out_b).reshape(E * M, K))[rows]
+    exp = bf16_vals(ref["out_b"])[rows]
+    rel = assert_fp_close(got, exp, "w2 alone")
+    assert rel < 2e-3, rel  # same inputs: only fp32-vs-fp64 accumulation differs
+
+
+def test_tiny_full(cuda, orc):
+    wl = syn.make_workload("tiny")
+    layer = _layer(wl, cuda)
+    h = _run_layer(layer, wl, cuda, dump=True)
+    ref = _full_check(orc, wl, layer, h)
+    _w2_alone(orc, wl, layer, ref, cuda)
+
+
+@pytest.mark.parametrize("shape", [
+    # T, K, N, E, k, M_max: several m-tiles with a ragged last one, K tail
+    # n-tile in w2 (K = 384), two w13 n-tiles
+    (250, 384, 256, 3, 2, 300),
+    # w2 split of the reduction (valid_shape_m hint forces several splits)
+    (40, 1024, 2048, 8, 2, 64),
+])
+def test_ragged_and_split(cuda, orc, shape):
+    T, K, N, E, k, M = shape
+    wl = _custom_workload(T, K, N, E, k, M, seed=T + K)
+    layer = _layer(wl, cuda, valid_shape_m=16 if N == 2048 else None)
+    h = _run_layer(layer, wl, cuda, dump=True)
+    ref = _full_check(orc, wl, layer, h)
+    _w2_alone(orc, wl, layer, ref, cuda)
+    # second call on the same buffers: same bits (deterministic, counters reset)
+    first = layer.out.clone()
+    _run_layer(layer, wl, cuda)
+    assert torch.equal(first, layer.out)
+
+
+@pytest.mark.parametrize("name,n_tok", [("mixtral_decode", 6), ("deepseek_decode", 6),
+                                        ("deepseek_prefill", 4)])
+def test_full_size_sampled(cuda, orc, name, n_tok):
+    """Full-size workloads in the bench's launch configuration; the oracle
+    recomputes a sample of tokens (every route of each) one by one."""
+    wl = syn.make_workload(name, weights_device="cuda")
+    c = wl["cfg"]
+    layer = _layer(wl, cuda)
+    h = _run_layer(layer, wl, cuda, dump=True)
+    rng = np.random.default_rng(42)
+    pad = wl["is_padding"].numpy()
+    cand = np.nonzero(pad == 0)[0]
+    tokens = np.sort(rng.choice(cand, size=n_tok, replace=False))
+    if pad.any():
+        tokens = np.concatenate([tokens, np.nonzero(pad)[0][:1]])
+    ref = oracle_sampled_forward(orc, wl, tokens, want_h=True)
+    assert np.array_equal(layer.route_slot.cpu().numpy(), ref["dispatch"]["route_slot"])
+    assert np.array_equal(layer.expert_num_tokens.cpu().numpy(),
+                          ref["dispatch"]["expert_num_tokens"])
+    M, N, K = c["M_max"], c["N"], c["K"]
+    g_rows = [e * M + s for (i, j, e, s) in ref["routes"]]
+    idx = torch.as_tensor(g_rows, dtype=torch.int64, device=cuda)
+    hg = bf16_vals(bf16_bits(h[idx]))
+    ob = bf16_vals(bf16_bits(layer.out_b.view(-1, K)[idx]))
+    for n_, (i, j, e, s) in enumerate(ref["routes"]):
+        r = ref["crow_of"][(i, j)]
+        assert_fp_close(hg[n_], bf16_vals(ref["h"][r]), f"h row {g_rows[n_]}")
+        assert_fp_close(ob[n_], bf16_vals(ref["out_b"][r]), f"out_b row {g_rows[n_]}")
+    out = bf16_vals(bf16_bits(layer.out))[tokens]
+    assert_fp_close(out, bf16_vals(ref["out"]), f"{name} output")
+    if pad.any():
+        assert np.all(out[-1] == 0), "padding token must be unrouted"

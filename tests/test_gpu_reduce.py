@@ -1,0 +1,59 @@
+"""GPU parity of moe_topk_reduce against the oracle (S8)."""
+import numpy as np
+import pytest
+import torch
+
+from moe_expert_layer_prepare_gb300 import binding as B
+from tests._util import bf16_bits, bf16_vals, need_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    need_cuda()
+    from moe_expert_layer_prepare_gb300 import build
+    build.build()
+    B.load()
+    return torch.device("cuda")
+
+
+@pytest.mark.parametrize("T,k,E,M,K", [(5, 1, 2, 4, 8), (77, 8, 16, 64, 7168),
+                                       (300, 2, 8, 128, 4104)])
+def test_reduce_vs_oracle(cuda, orc, T, k, E, M, K):
+    rng = np.random.default_rng(T + K)
+    out_b = torch.randn(E, M, K).to(torch.bfloat16)
+    ids = rng.integers(-1, E, size=(T, k)).astype(np.int64)
+    slots = rng.integers(-1, M, size=(T, k)).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    dev = torch.device("cuda")
+    out = torch.full((T, K), 3.0, dtype=torch.bfloat16, device=dev)
+    B.moe_topk_reduce(out_b.to(dev), torch.from_numpy(ids).to(dev),
+                      torch.from_numpy(slots).to(dev), torch.from_numpy(w).to(dev), out)
+    torch.cuda.synchronize()
+    ref = orc.topk_reduce(bf16_bits(out_b).reshape(E * M, K), ids, slots, w, M)
+    got = bf16_vals(bf16_bits(out)).astype(np.float64)
+    rv = bf16_vals(ref).astype(np.float64)
+    # fp32 sum vs the oracle's fp64 sum: one bf16 rounding apart at most
+    assert np.all(np.abs(got - rv) <= np.abs(rv) * 2.0 ** -7 + 1e-30)
+    none = np.all((ids < 0) | (slots < 0), axis=1)
+    assert np.all(got[none] == 0)
+    if k == 1:
+        wt = np.where((ids[:, 0] >= 0) & (slots[:, 0] >= 0), w[:, 0], 0)
+        assert np.all(wt >= 0)
+
+
+def test_reduce_gather_exact(cuda):
+    E, M, K, T = 4, 16, 512, 40
+    out_b = torch.randn(E, M, K).to(torch.bfloat16)
+    rng = np.random.default_rng(1)
+    ids = rng.integers(0, E, size=(T, 1)).astype(np.int64)
+    slots = rng.integers(0, M, size=(T, 1)).astype(np.int32)
+    dev = torch.device("cuda")
+    out = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    B.moe_topk_reduce(out_b.to(dev), torch.from_numpy(ids).to(dev),
+                      torch.from_numpy(slots).to(dev),
+                      torch.ones((T, 1), dtype=torch.float32, device=dev), out)
+    torch.cuda.synchronize()
+    exp = out_b[torch.from_numpy(ids[:, 0]), torch.from_numpy(slots[:, 0].astype(np.int64))]
+    assert torch.equal(out.cpu(), exp)
