@@ -424,9 +424,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto epi_sync = [&]() {
       __syncwarp();
       if (lane == 0) mbar_arrive(epi_bar);
-      if (!mbar_wait(epi_bar, epi_phase, abort_flag, p.status)) ok = false;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(epi_bar, epi_phase, abort_flag, p.status)))
+        ok = false;
       epi_phase ^= 1u;
-      __syncwarp();
     };
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       const Unit w = decode_unit(p, prefix, u, cnt);
@@ -455,7 +455,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float sa = __uint_as_float(max(ea, 1u) << 23);
         const float s0 = sa * __ldg(ws0 + kb);
         const float s1 = sa * __ldg(ws1 + kb);
-        if (!mbar_wait(tfull0 + 8 * ab, aphase, abort_flag, p.status)) {
+        // warp-uniform outcome; also reconverges the warp before the
+        // .sync.aligned TMEM loads
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * ab, aphase, abort_flag, p.status))) {
           ok = false;
           break;
         }
