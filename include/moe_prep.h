@@ -155,6 +155,34 @@ moe_status_t moe_prepare_inputs(const moe_prepare_args_t* args, void* stream);
 size_t moe_prepare_workspace_size(int64_t num_tokens, int64_t top_k, int64_t num_experts);
 
 /* ------------------------------------------------------------------------ */
+/* moe_prepare_inputs_noalloc                                                */
+/*                                                                           */
+/* No counterpart on the pages: an addition of this library for callers that */
+/* cannot allocate device memory -- a plugin that is handed only its input   */
+/* and output buffers, code running under a CUDA graph capture where its      */
+/* framework forbids allocation, or a process held to a fixed device-memory  */
+/* budget that must never call cudaMalloc (which can also synchronise the    */
+/* device).                                                                  */
+/*                                                                           */
+/* Same arguments, checks and results as moe_prepare_inputs, except that the */
+/* dispatch scratch comes from a fixed array of                              */
+/* MOE_PREPARE_NOALLOC_SCRATCH_BYTES bytes inside the library (present on    */
+/* every GPU that loads it, until the process exits); args->workspace and    */
+/* args->workspace_bytes are ignored.  A problem whose                       */
+/* moe_prepare_workspace_size() exceeds that size returns                    */
+/* MOE_ERR_WORKSPACE before anything is enqueued.  Nothing is allocated: no  */
+/* cudaMalloc/cudaFree or allocating library call.  The array's device       */
+/* address is looked up on the first call made with a device current, so    */
+/* make that first call before any stream capture.  Every call on a device   */
+/* shares the one array and finds the previous call's contents there (each   */
+/* call clears what must start at zero); calls that may overlap on the GPU   */
+/* race on it and must be serialised by the caller.                          */
+/* ------------------------------------------------------------------------ */
+#define MOE_PREPARE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+moe_status_t moe_prepare_inputs_noalloc(const moe_prepare_args_t* args, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* moe_batched_experts                                                       */
 /*                                                                           */
 /* Defined by BatchedHummingGroupedExperts.apply and                         */

@@ -85,6 +85,8 @@ def load():
     lib.moe_prepare_inputs.argtypes = [ctypes.POINTER(PrepareArgs), _vp]
     lib.moe_prepare_workspace_size.restype = _sz
     lib.moe_prepare_workspace_size.argtypes = [_i64, _i64, _i64]
+    lib.moe_prepare_inputs_noalloc.restype = ctypes.c_int
+    lib.moe_prepare_inputs_noalloc.argtypes = [ctypes.POINTER(PrepareArgs), _vp]
     lib.moe_batched_experts.restype = ctypes.c_int
     lib.moe_batched_experts.argtypes = [ctypes.POINTER(ExpertsArgs), _vp]
     lib.moe_batched_experts_workspace_size.restype = _sz
@@ -178,6 +180,62 @@ def moe_prepare_inputs(hidden, topk_ids, topk_weights, x, x_sf, topk_idx_out, to
         a.workspace, a.workspace_bytes = _ptr(ws), ws.numel() * ws.element_size()
     a.device_status = _ptr(device_status)
     _check("moe_prepare_inputs", load().moe_prepare_inputs(ctypes.byref(a), _stream(stream)))
+
+
+def moe_prepare_inputs_noalloc(hidden, topk_ids, topk_weights, x, x_sf, topk_idx_out,
+                               topk_weights_out, is_padding=None, sf_mode=MOE_SF_UE8M0_PACKED,
+                               eplb=None, dispatch=None, device_status=None, stream=None):
+    """Staging + dispatch for callers that cannot allocate device memory.
+
+    Same arguments as ``moe_prepare_inputs`` except that ``dispatch`` needs no
+    ``workspace``: the scratch of the dispatch is a fixed array inside the
+    library (MOE_PREPARE_NOALLOC_SCRATCH_BYTES, 4 MiB, per GPU).  Calls on one
+    device share that array, so calls that may overlap on the GPU must be
+    serialised; the first call on a device looks the array up, so make it
+    before any stream capture.
+    """
+    T, K = hidden.shape
+    a = PrepareArgs()
+    a.num_tokens, a.hidden_size = T, K
+    a.top_k = topk_ids.shape[1] if topk_ids.dim() == 2 else 0
+    a.hidden, a.hidden_stride0 = _ptr(hidden), hidden.stride(0)
+    a.topk_ids = _ptr(topk_ids)
+    a.topk_ids_dtype = MOE_IDS_INT64 if topk_ids.dtype == torch.int64 else MOE_IDS_INT32
+    a.topk_ids_stride0, a.topk_ids_stride1 = topk_ids.stride(0), topk_ids.stride(1)
+    a.topk_weights = _ptr(topk_weights)
+    a.topk_weights_dtype = MOE_WEIGHTS_BF16 if topk_weights.dtype == torch.bfloat16 else \
+        MOE_WEIGHTS_FP32
+    a.topk_weights_stride0, a.topk_weights_stride1 = topk_weights.stride(0), topk_weights.stride(1)
+    if is_padding is not None:
+        a.is_padding, a.is_padding_stride0 = _ptr(is_padding), is_padding.stride(0)
+    a.x, a.x_stride0 = _ptr(x), x.stride(0)
+    a.sf_mode = sf_mode
+    if x_sf is not None:
+        a.x_sf, a.x_sf_stride0 = _ptr(x_sf), x_sf.stride(0)
+        a.x_sf_stride1 = x_sf.stride(1) if x_sf.dim() > 1 else 1
+    a.topk_idx_out = _ptr(topk_idx_out)
+    a.topk_idx_out_stride0, a.topk_idx_out_stride1 = topk_idx_out.stride(0), topk_idx_out.stride(1)
+    a.topk_weights_out = _ptr(topk_weights_out)
+    a.topk_weights_out_stride0 = topk_weights_out.stride(0)
+    a.topk_weights_out_stride1 = topk_weights_out.stride(1)
+    if eplb:
+        l2p = eplb["logical_to_physical"]
+        a.logical_to_physical, a.num_logical, a.map_stride = _ptr(l2p), l2p.shape[0], l2p.stride(0)
+        a.logical_replica_count = _ptr(eplb["logical_replica_count"])
+        load_t = eplb.get("expert_load")
+        if load_t is not None:
+            a.expert_load, a.num_physical = _ptr(load_t), load_t.numel()
+        a.should_record = _ptr(eplb.get("should_record"))
+        a.num_unpadded_tokens = _ptr(eplb.get("num_unpadded_tokens"))
+    if dispatch:
+        a.num_experts = dispatch["num_experts"]
+        a.max_tokens_per_expert = dispatch["max_tokens_per_expert"]
+        a.x_b, a.sf_b = _ptr(dispatch["x_b"]), _ptr(dispatch["sf_b"])
+        a.expert_num_tokens = _ptr(dispatch["expert_num_tokens"])
+        a.route_slot = _ptr(dispatch["route_slot"])
+    a.device_status = _ptr(device_status)
+    _check("moe_prepare_inputs_noalloc",
+           load().moe_prepare_inputs_noalloc(ctypes.byref(a), _stream(stream)))
 
 
 def moe_batched_experts(output, hidden, a_scale, w13, w13_scale, w2, w2_scale,
