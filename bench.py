@@ -249,10 +249,12 @@ def bench_ours(args, world, rank, local):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     for i in range(K):
         flush.zero_()  # L2 flush between timed steps (outside the events)
         step(evs[i])
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     ck = clocks.stop()
     stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
@@ -367,12 +369,14 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
            for _ in range(Ks)]
     barrier(world)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     for i in range(Ks):
         flush.zero_()
         evs[i][0].record(s)
         step()
         evs[i][1].record(s)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     ck = clocks.stop()
     ms = max_over_ranks(world, float(np.mean([a.elapsed_time(b) for a, b in evs])))

@@ -50,8 +50,17 @@ constexpr int A_BYTES = BM * BK;              // 16 KB
 constexpr int B_BYTES = BN * BK;              // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int A_BOX_ROWS = 32;
-constexpr int NUM_THREADS = 320;              // 10 warps
+constexpr int NUM_THREADS = 384;              // 12 warps = 3 warpgroups
+constexpr int EPI_WARP0 = 4;                  // warpgroups 1-2 are the epilogue
 constexpr int EPI_WARPS = 8;
+// Register split (setmaxnreg): the kernel is compiled for 168 registers per
+// thread (384 x 168 = 64512); warpgroup 0 (TMA, MMA, two idle warps) drops to
+// 40 and the two epilogue warpgroups rise to 232: 128 x 40 + 256 x 232 = 64512.
+constexpr int LAUNCH_REGS = 168;
+constexpr int PRODUCER_REGS = 40;
+constexpr int EPILOGUE_REGS = 232;
+static_assert(128 * PRODUCER_REGS + 256 * EPILOGUE_REGS <= NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
 constexpr int MAX_EXPERTS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -118,8 +127,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: false when the CTA aborted or this wait exceeded ~2 s.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
@@ -197,6 +206,23 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// Wait for outstanding TMEM loads; the 32 destination registers of the last
+// load are read-write operands so that no use of them can move above the wait.
+#define TMEM_WAIT_PIN32(r)                                                                      \
+  asm volatile("tcgen05.wait::ld.sync.aligned;"                                                 \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),        \
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),      \
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),  \
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),  \
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),  \
+                 "+r"(r[30]), "+r"(r[31])                                                       \
+               :                                                                                \
+               : "memory")
+
+#define FMA32(dst, r, s)                                                  \
+  _Pragma("unroll") for (int i_ = 0; i_ < 32; ++i_) (dst)[i_] =           \
+      fmaf(__uint_as_float((r)[i_]), (s), (dst)[i_])
 
 
 // ------------------------------------------------------------------ schedule
@@ -311,106 +337,108 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
   const int total_units = prefix[p.E] * p.n_tiles * p.splits;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- TMA
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_mask = 0, issued_phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit w = decode_unit(p, prefix, u, cnt);
-        const int a_row0 = w.e * p.M_max + w.mt * BM;
-        const int n_boxes = (w.rows + A_BOX_ROWS - 1) / A_BOX_ROWS;
-        const uint32_t tx = (uint32_t)(n_boxes * A_BOX_ROWS * BK + B_BYTES);
-        int b_row0, b_row1;
-        if constexpr (W13) {
-          b_row0 = w.e * p.b_rows + w.nt * 128;
-          b_row1 = w.e * p.b_rows + p.N + w.nt * 128;
-        } else {
-          b_row0 = w.e * p.b_rows + w.nt * 256;
-          b_row1 = b_row0 + 128;
-        }
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
+  if (warp < EPI_WARP0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PRODUCER_REGS));
+    if (warp == 0) {
+      // ---------------------------------------------------------------- TMA
+      if (lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+          const Unit w = decode_unit(p, prefix, u, cnt);
+          const int a_row0 = w.e * p.M_max + w.mt * BM;
+          const int n_boxes = (w.rows + A_BOX_ROWS - 1) / A_BOX_ROWS;
+          const uint32_t tx = (uint32_t)(n_boxes * A_BOX_ROWS * BK + B_BYTES);
+          int b_row0, b_row1;
+          if constexpr (W13) {
+            b_row0 = w.e * p.b_rows + w.nt * 128;
+            b_row1 = w.e * p.b_rows + p.N + w.nt * 128;
+          } else {
+            b_row0 = w.e * p.b_rows + w.nt * 256;
+            b_row1 = b_row0 + 128;
           }
-          const uint32_t fb = full0 + 8 * stage;
-          mbar_expect_tx(fb, tx);
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
-          for (int i = 0; i < n_boxes; ++i)
-            tma_load_2d(sa + i * A_BOX_ROWS * BK, &tmA, kb * BK, a_row0 + i * A_BOX_ROWS, fb);
-          tma_load_2d(sb, &tmB, kb * BK, b_row0, fb);
-          tma_load_2d(sb + 128 * BK, &tmB, kb * BK, b_row1, fb);
-          issued_mask |= 1u << stage;
-          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_expect_tx(fb, tx);
+            const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t sb = sa + A_BYTES;
+            for (int i = 0; i < n_boxes; ++i)
+              tma_load_2d(sa + i * A_BOX_ROWS * BK, &tmA, kb * BK, a_row0 + i * A_BOX_ROWS, fb);
+            tma_load_2d(sb, &tmB, kb * BK, b_row0, fb);
+            tma_load_2d(sb + 128 * BK, &tmB, kb * BK, b_row1, fb);
+            issued_mask |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        // Drain: every issued stage's copy must have landed before exit.
+        for (int s = 0; s < STAGES; ++s) {
+          if (issued_mask & (1u << s)) {
+            volatile int never = 0;
+            mbar_wait(full0 + 8 * s, (issued_phase >> s) & 1u, &never, p.status);
           }
         }
       }
-      // Drain: every issued stage's copy must have landed before exit.
-      for (int s = 0; s < STAGES; ++s) {
-        if (issued_mask & (1u << s)) {
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int ab = 0;
+        uint32_t aphase = 0;
+        bool ok = true;
+        bool any = false;
+        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+          const Unit w = decode_unit(p, prefix, u, cnt);
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!mbar_wait(tempty0 + 8 * ab, aphase ^ 1u, abort_flag, p.status) ||
+                !mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+            const uint64_t adesc = sw128_desc(sa);
+            const uint64_t bdesc = sw128_desc(sa + A_BYTES);
+            const uint32_t d = tmem_base + (uint32_t)(ab * BN);
+  #pragma unroll
+            for (int k = 0; k < BK / 32; ++k)
+              mma_f8(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), k > 0 ? 1u : 0u);
+            mma_commit(empty0 + 8 * stage);
+            mma_commit(tfull0 + 8 * ab);
+            any = true;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            ab ^= 1;
+            if (ab == 0) aphase ^= 1u;
+          }
+        }
+        if (any) {
+          // all MMAs of this CTA complete before TMEM is freed
+          mma_commit(mma_done);
           volatile int never = 0;
-          uint32_t dummy_status = 0;
-          (void)dummy_status;
-          mbar_wait(full0 + 8 * s, (issued_phase >> s) & 1u, &never, p.status);
+          mbar_wait(mma_done, 0, &never, p.status);
         }
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int ab = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      bool any = false;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit w = decode_unit(p, prefix, u, cnt);
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(tempty0 + 8 * ab, aphase ^ 1u, abort_flag, p.status) ||
-              !mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint64_t adesc = sw128_desc(sa);
-          const uint64_t bdesc = sw128_desc(sa + A_BYTES);
-          const uint32_t d = tmem_base + (uint32_t)(ab * BN);
-#pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            mma_f8(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), k > 0 ? 1u : 0u);
-          mma_commit(empty0 + 8 * stage);
-          mma_commit(tfull0 + 8 * ab);
-          any = true;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          ab ^= 1;
-          if (ab == 0) aphase ^= 1u;
-        }
-      }
-      if (any) {
-        // all MMAs of this CTA complete before TMEM is freed
-        mma_commit(mma_done);
-        volatile int never = 0;
-        mbar_wait(mma_done, 0, &never, p.status);
       }
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPILOGUE_REGS));
     // ---------------------------------------------------------------- epilogue
-    const int q = warp & 3;              // TMEM lane quarter
-    const int h = (warp - 2) >> 2;       // column half
+    const int q = warp & 3;                    // TMEM lane quarter
+    const int h = (warp - EPI_WARP0) >> 2;     // column half
     const int row_local = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
     int ab = 0;
@@ -428,9 +456,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = false;
       epi_phase ^= 1u;
     };
+    // TMEM column offsets of this thread's four 32-column groups.
+    uint32_t cg[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      cg[c] = W13 ? (uint32_t)((c < 2 ? 0 : 128) + h * 64 + (c & 1) * 32)
+                  : (uint32_t)(h * 128 + c * 32);
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       const Unit w = decode_unit(p, prefix, u, cnt);
       const bool row_ok = row_local < w.rows;
+      const bool warp_active = q * 32 < w.rows;   // warp-uniform
       const int64_t grow = (int64_t)w.e * p.M_max + (int64_t)w.mt * BM + row_local;
       int nb0, nb1;
       if constexpr (W13) {
@@ -449,45 +484,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
 
+      // scales of the slab, loaded one slab ahead
+      uint32_t aw = row_ok ? __ldg(asf_row + (w.kb0 >> 2)) : 0x7F7F7F7Fu;
+      float wsc0 = __ldg(ws0 + w.kb0), wsc1 = __ldg(ws1 + w.kb0);
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        const uint32_t word = row_ok ? __ldg(asf_row + (kb >> 2)) : (127u << (8 * (kb & 3)));
-        const uint32_t ea = (word >> (8 * (kb & 3))) & 0xFFu;
+        const uint32_t ea = (aw >> (8 * (kb & 3))) & 0xFFu;
         const float sa = __uint_as_float(max(ea, 1u) << 23);
-        const float s0 = sa * __ldg(ws0 + kb);
-        const float s1 = sa * __ldg(ws1 + kb);
+        const float s0 = sa * wsc0;
+        const float s1 = sa * wsc1;
+        if (kb + 1 < w.kb1) {
+          if (((kb + 1) & 3) == 0 && row_ok) aw = __ldg(asf_row + ((kb + 1) >> 2));
+          wsc0 = __ldg(ws0 + kb + 1);
+          wsc1 = __ldg(ws1 + kb + 1);
+        }
         // warp-uniform outcome; also reconverges the warp before the
         // .sync.aligned TMEM loads
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * ab, aphase, abort_flag, p.status))) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t base = lane_addr + (uint32_t)(ab * BN);
-        uint32_t r[32];
-        if constexpr (W13) {
-          // gate columns [h*64, h*64+64), up columns [128 + h*64, ...)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t col = (c < 2) ? (uint32_t)(h * 64 + c * 32)
-                                         : (uint32_t)(128 + h * 64 + (c - 2) * 32);
-            TMEM_LD32(base + col, r);
-            tmem_wait_ld();
-            const float s = (c < 2) ? s0 : s1;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), s, acc[c * 32 + i]);
-          }
+        if (warp_active) {
+          tc_fence_after();
+          const uint32_t base = lane_addr + (uint32_t)(ab * BN);
+          uint32_t ra[32], rb[32];
+          // ping-pong: the load of one group overlaps the FMAs of the other
+          TMEM_LD32(base + cg[0], ra);
+          TMEM_WAIT_PIN32(ra);
+          TMEM_LD32(base + cg[1], rb);
+          FMA32(acc + 0, ra, s0);
+          TMEM_WAIT_PIN32(rb);
+          TMEM_LD32(base + cg[2], ra);
+          FMA32(acc + 32, rb, s0);
+          TMEM_WAIT_PIN32(ra);
+          TMEM_LD32(base + cg[3], rb);
+          FMA32(acc + 64, ra, W13 ? s1 : s0);
+          TMEM_WAIT_PIN32(rb);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
+          FMA32(acc + 96, rb, W13 ? s1 : s0);
         } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            TMEM_LD32(base + (uint32_t)(h * 128 + c * 32), r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), s0, acc[c * 32 + i]);
-          }
+          // no row of this warp holds a token: nothing to read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
         ab ^= 1;
         if (ab == 0) aphase ^= 1u;
       }
@@ -571,7 +611,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           __threadfence();
           epi_sync();
           int32_t* ctr = p.counters + ((int64_t)w.e * p.mt_max + w.mt) * p.n_tiles + w.nt;
-          if (tid == 2 * 32) {
+          if (tid == EPI_WARP0 * 32) {
             const int prev = atomicAdd(ctr, 1);
             *s_flag = (prev == p.splits - 1) ? 1 : 0;
           }
@@ -579,7 +619,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (*s_flag) {
             __threadfence();
             if (row_ok && cols_ok) {
-              float sum[128];
+              float* sum = acc;  // partials are summed in split order
 #pragma unroll
               for (int i = 0; i < 128; ++i) sum[i] = 0.0f;
               for (int s = 0; s < p.splits; ++s) {
@@ -604,7 +644,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 st_v4(dst + i, v);
               }
             }
-            if (tid == 2 * 32) *ctr = 0;
+            if (tid == EPI_WARP0 * 32) *ctr = 0;
           }
         }
       }
@@ -666,24 +706,21 @@ static int64_t est_mtiles(int64_t E, int64_t M_max, int64_t vsm) {
   return est < cap ? est : cap;
 }
 
-// Reduction splits of the w2 GEMM: best wave efficiency over the SMs, at
-// least 4 slabs per split, every split non-empty.
+// Reduction splits of the w2 GEMM.  The decode GEMMs stream weights: once the
+// output tiles alone keep about three quarters of the SMs busy, the active
+// CTAs already saturate HBM and a split only adds partial-sum traffic, so the
+// reduction is split only when there are fewer tiles than that (enough splits
+// to cover ~90% of the SMs, at least 4 slabs each, every split non-empty).
 static int choose_splits(int64_t units_base, int KB, int sms) {
-  int best = 1;
-  double best_eff = -1.0;
-  for (int s = 1; s <= 16; ++s) {
-    const int per = (KB + s - 1) / s;
-    if (per < 4 && s > 1) break;
-    if ((int64_t)(s - 1) * per >= KB) continue;
-    const int64_t units = units_base * s;
-    const int64_t waves = (units + sms - 1) / sms;
-    const double eff = (double)units / (double)(waves * sms);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = s;
-    }
+  if (units_base <= 0 || units_base * 4 >= (int64_t)sms * 3) return 1;
+  int64_t want = ((int64_t)sms * 9 / 10 + units_base - 1) / units_base;
+  int sp = (int)(want > 16 ? 16 : want);
+  while (sp > 1) {
+    const int per = (KB + sp - 1) / sp;
+    if (per >= 4 && (int64_t)(sp - 1) * per < KB) break;
+    --sp;
   }
-  return best;
+  return sp < 1 ? 1 : sp;
 }
 
 static int w2_splits(int64_t E, int64_t M_max, int64_t K, int64_t N, int64_t vsm) {
@@ -750,6 +787,15 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
     if (e1 != cudaSuccess || e2 != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "GEMM smem attribute: %s",
                        cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+    // The in-kernel register split assumes the launch allocation below.
+    cudaFuncAttributes fa13, fa2;
+    if (cudaFuncGetAttributes(&fa13, moe::grouped_gemm_kernel<true>) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa2, moe::grouped_gemm_kernel<false>) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaFuncGetAttributes failed for the GEMM kernels");
+    if (fa13.numRegs != moe::LAUNCH_REGS || fa2.numRegs != moe::LAUNCH_REGS)
+      return set_error(MOE_ERR_UNSUPPORTED,
+                       "GEMM kernels built with %d/%d registers per thread; the register "
+                       "split needs exactly %d", fa13.numRegs, fa2.numRegs, moe::LAUNCH_REGS);
     attr_done[0] = true;
   }
   // Upper bound of the work units: every expert full.  Persistent grid.

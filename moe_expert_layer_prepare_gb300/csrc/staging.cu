@@ -14,10 +14,12 @@
 //                  block to finish turns the histograms into per-block
 //                  exclusive offsets (column scan over blocks) and writes
 //                  expert_num_tokens.
-//   quant_kernel : one warp per (token, 4 groups = 512 elements): 16-byte
-//                  loads, warp-shuffle amax over the 8 lanes of a group, packed
-//                  fp8 stores, one packed exponent word per task; optionally
-//                  the same bytes are stored into each routed slot of x_b.
+//   quant_kernel : one warp per (token, 4 groups = 512 elements): two
+//                  16-byte loads per lane, each covering 512 contiguous bytes
+//                  per warp, warp-shuffle amax over the 16 lanes of a group,
+//                  packed fp8 stores, one packed exponent word per task;
+//                  optionally the same bytes are stored into each routed slot
+//                  of x_b.
 //                  Without dispatch the repack is folded into this kernel.
 #include <cstdio>
 
@@ -182,9 +184,53 @@ __global__ void __launch_bounds__(1024) route_kernel(StageParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// quant_kernel: one warp per (token t, word w) task = groups 4w .. 4w+3.
-// Lane l covers 16 elements of group 4w + l/8.
+// quant_kernel: one warp per (token t, word w) task = groups 4w .. 4w+3
+// (512 elements).  Each of the two 16-byte loads of the warp covers 512
+// contiguous bytes: load A holds groups 4w (lanes 0-15) and 4w+1 (lanes
+// 16-31), load B groups 4w+2 and 4w+3.  A group's amax is reduced over its 16
+// lanes; every lane stores its 8 fp8 codes of each load (256 contiguous bytes
+// per warp store).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float amax8(uint4 v, float f[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
+    f[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
+    m = fmaxf(m, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+  }
+  // reduce over the 16 lanes that share the group
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  return m;
+}
+
+template <int SF_MODE>
+__device__ __forceinline__ uint2 quant8(const float f[8], float amax, uint32_t& code) {
+  float inv;
+  if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
+    code = ue8m0_exponent(amax);
+    inv = __frcp_rn(__uint_as_float(code << 23));
+  } else {
+    const float s = __fdiv_rn(fmaxf(amax, 1.0e-4f), 448.0f);
+    code = __float_as_uint(s);
+    inv = __frcp_rn(s);
+  }
+  uint2 q;
+  q.x = pack4_e4m3(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                   __fmul_rn(f[3], inv));
+  q.y = pack4_e4m3(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),
+                   __fmul_rn(f[7], inv));
+  return q;
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+  asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
 template <int SF_MODE, bool REPACK, bool DISPATCH, typename IdT, typename WT>
 __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
   const int lane = threadIdx.x & 31;
@@ -201,76 +247,52 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
       repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
   }
 
-  const int grp = lane >> 3;
-  const int sub = lane & 7;
+  const int half = lane >> 4;  // group within each load
   const int64_t tasks = p.T * p.W;
   for (int64_t task = gwarp; task < tasks; task += nwarps) {
     const int64_t t = task / p.W;
     const int64_t w = task - t * p.W;
-    const int64_t g = 4 * w + grp;
-    const bool active = g < p.G;
-    const int64_t col = g * kGroup + sub * 16;
-    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-    if (active) {
-      const uint16_t* src = p.hidden + t * p.hs0 + col;
-      v0 = ld_stream_v4(src);
-      v1 = ld_stream_v4(src + 8);
-    }
+    const int64_t gA = 4 * w + half;      // group of load A
+    const int64_t gB = 4 * w + 2 + half;  // group of load B
+    const bool actA = gA < p.G, actB = gB < p.G;
+    const int64_t e0 = 4 * w * kGroup;    // first element of the task
+    const int64_t offA = e0 + lane * 8, offB = e0 + 256 + lane * 8;
+    const uint16_t* src = p.hidden + t * p.hs0;
+    uint4 vA = make_uint4(0, 0, 0, 0), vB = vA;
+    if (actA) vA = ld_stream_v4(src + offA);
+    if (actB) vB = ld_stream_v4(src + offB);
     if constexpr (SF_MODE == MOE_SF_NONE) {
-      if (active) {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(p.x) + t * p.xs0 + col;
-        st_v4(dst, v0);
-        st_v4(dst + 8, v1);
-      }
+      uint16_t* dst = reinterpret_cast<uint16_t*>(p.x) + t * p.xs0;
+      if (actA) st_v4(dst + offA, vA);
+      if (actB) st_v4(dst + offB, vB);
       continue;
     } else {
-      float f[16];
-      const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        f[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
-        f[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
-      }
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      uint32_t code;
-      float inv;
-      if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
-        code = ue8m0_exponent(amax);
-        inv = __frcp_rn(__uint_as_float(code << 23));
-      } else {
-        float s = __fdiv_rn(fmaxf(amax, 1.0e-4f), 448.0f);
-        code = __float_as_uint(s);
-        inv = __frcp_rn(s);
-      }
-      uint4 q;
-      q.x = pack4_e4m3(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
-                       __fmul_rn(f[3], inv));
-      q.y = pack4_e4m3(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),
-                       __fmul_rn(f[7], inv));
-      q.z = pack4_e4m3(__fmul_rn(f[8], inv), __fmul_rn(f[9], inv), __fmul_rn(f[10], inv),
-                       __fmul_rn(f[11], inv));
-      q.w = pack4_e4m3(__fmul_rn(f[12], inv), __fmul_rn(f[13], inv), __fmul_rn(f[14], inv),
-                       __fmul_rn(f[15], inv));
-      if (active) st_v4(p.x + t * p.xs0 + col, q);
+      float fA[8], fB[8];
+      const float mA = amax8(vA, fA);
+      const float mB = amax8(vB, fB);
+      uint32_t cA, cB;
+      const uint2 qA = quant8<SF_MODE>(fA, mA, cA);
+      const uint2 qB = quant8<SF_MODE>(fB, mB, cB);
+      uint8_t* xrow = p.x + t * p.xs0;
+      if (actA) st_v2(xrow + offA, qA);
+      if (actB) st_v2(xrow + offB, qB);
 
       uint32_t word = 0;
       if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
-        const uint32_t mine = active ? code : 0u;
-        const uint32_t e0 = __shfl_sync(0xFFFFFFFFu, mine, 0);
-        const uint32_t e1 = __shfl_sync(0xFFFFFFFFu, mine, 8);
-        const uint32_t e2 = __shfl_sync(0xFFFFFFFFu, mine, 16);
-        const uint32_t e3 = __shfl_sync(0xFFFFFFFFu, mine, 24);
-        word = e0 | (e1 << 8) | (e2 << 16) | (e3 << 24);
+        const uint32_t a = actA ? cA : 0u, b = actB ? cB : 0u;
+        const uint32_t e0w = __shfl_sync(0xFFFFFFFFu, a, 0);
+        const uint32_t e1w = __shfl_sync(0xFFFFFFFFu, a, 16);
+        const uint32_t e2w = __shfl_sync(0xFFFFFFFFu, b, 0);
+        const uint32_t e3w = __shfl_sync(0xFFFFFFFFu, b, 16);
+        word = e0w | (e1w << 8) | (e2w << 16) | (e3w << 24);
         if (lane == 0)
           reinterpret_cast<uint32_t*>(p.x_sf)[t * p.sfs0 + w * p.sfs1] = word;
       } else {
-        if (active && sub == 0)
-          reinterpret_cast<float*>(p.x_sf)[t * p.sfs0 + g * p.sfs1] = __uint_as_float(code);
+        if ((lane & 15) == 0) {
+          float* sf = reinterpret_cast<float*>(p.x_sf) + t * p.sfs0;
+          if (actA) sf[gA * p.sfs1] = __uint_as_float(cA);
+          if (actB) sf[gB * p.sfs1] = __uint_as_float(cB);
+        }
       }
 
       if constexpr (DISPATCH) {
@@ -284,9 +306,10 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
             if (slot >= p.M_max) slot = -1;
           }
           if (slot >= 0) {
-            const int64_t row = e * p.M_max + slot;
-            if (active) st_v4(p.x_b + row * K + col, q);
-            if (lane == 0) p.sf_b[row * p.W + w] = (int32_t)word;
+            uint8_t* brow = p.x_b + (e * p.M_max + slot) * K;
+            if (actA) st_v2(brow + offA, qA);
+            if (actB) st_v2(brow + offB, qB);
+            if (lane == 0) p.sf_b[(e * p.M_max + slot) * p.W + w] = (int32_t)word;
           }
           if (w == 0 && lane == 0) p.route_slot[r] = (int32_t)slot;
         }

@@ -144,7 +144,8 @@ def test_reduce_gather_and_convex(orc):
     T, K, M = 6, 256, 8
     E = 3
     rng = np.random.default_rng(3)
-    ob = _bf16_bits(torch.randn(E * M, K).to(torch.bfloat16))
+    ob = _bf16_bits(torch.from_numpy(rng.standard_normal((E * M, K), dtype=np.float32))
+                    .to(torch.bfloat16))
     ids = np.array([[0], [1], [2], [-1], [1], [0]], np.int64)
     slot = np.array([[0], [3], [7], [-1], [2], [-1]], np.int32)
     w = np.ones((T, 1), np.float32)
