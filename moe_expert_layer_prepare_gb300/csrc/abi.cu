@@ -31,6 +31,25 @@ int num_sms() {
   return cached[dev];
 }
 
+// Resident blocks per SM of a kernel at a block size (cached per kernel).
+int resident_blocks(const void* kernel, int block) {
+  static const void* keys[32] = {};
+  static int vals[32] = {};
+  for (int i = 0; i < 32; ++i) {
+    if (keys[i] == kernel) return vals[i];
+    if (keys[i] == nullptr) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, 0) != cudaSuccess ||
+          n < 1)
+        n = 1;
+      keys[i] = kernel;
+      vals[i] = n;
+      return n;
+    }
+  }
+  return 1;
+}
+
 size_t prepare_workspace_size(int64_t T, int64_t k, int64_t E);
 moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s);
 moe_status_t launch_topk_reduce(const void* expert_out, int64_t E, int64_t M_max, int64_t K,
@@ -86,6 +105,8 @@ moe_status_t moe_prepare_inputs(const moe_prepare_args_t* a, void* stream) {
   if (!aligned16(a->hidden) || (a->hidden_stride0 * 2) % 16 != 0 || !aligned16(a->x) ||
       (a->x_stride0 * x_elem) % 16 != 0)
     return set_error(MOE_ERR_ALIGNMENT, "hidden/x rows must start on 16-byte boundaries");
+  if (a->num_tokens * ((G + 3) / 4) >= ((int64_t)1 << 31))
+    return set_error(MOE_ERR_UNSUPPORTED, "num_tokens * ceil(K/512) must be below 2^31");
   if (a->sf_mode == MOE_SF_UE8M0_PACKED && a->x_sf_stride1 < 1 && (G + 3) / 4 > 1)
     return set_error(MOE_ERR_SHAPE, "x_sf stride1 must be positive");
   if (a->logical_to_physical != nullptr) {
@@ -190,6 +211,8 @@ moe_status_t moe_topk_reduce(const void* expert_out, int64_t num_experts,
   if (num_experts <= 0 || max_tokens_per_expert <= 0)
     return set_error(MOE_ERR_INVALID_ARGUMENT, "num_experts and max_tokens_per_expert must be positive");
   if (hidden_size % 8 != 0) return set_error(MOE_ERR_SHAPE, "hidden_size must be a multiple of 8");
+  if (num_tokens * ((hidden_size + 255) / 256) >= ((int64_t)1 << 31))
+    return set_error(MOE_ERR_UNSUPPORTED, "num_tokens * ceil(K/256) must be below 2^31");
   if (!expert_out || !out || (top_k > 0 && (!topk_idx || !route_slot || !topk_weights)))
     return set_error(MOE_ERR_INVALID_ARGUMENT, "a required pointer is NULL");
   if (!aligned16(expert_out) || !aligned16(out))

@@ -220,9 +220,22 @@ __device__ __forceinline__ void tmem_wait_ld() {
                :                                                                                \
                : "memory")
 
-#define FMA32(dst, r, s)                                                  \
-  _Pragma("unroll") for (int i_ = 0; i_ < 32; ++i_) (dst)[i_] =           \
-      fmaf(__uint_as_float((r)[i_]), (s), (dst)[i_])
+// dst[i] += r[i] * s for 32 columns, two lanes per instruction (paired fp32
+// FMA, round-to-nearest like fmaf).
+__device__ __forceinline__ void fma2(float& d0, float& d1, uint32_t a0, uint32_t a1, float s) {
+  asm("{ .reg .b64 a, b, c;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %4};\n\t"
+      "mov.b64 c, {%0, %1};\n\t"
+      "fma.rn.f32x2 c, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, c; }"
+      : "+f"(d0), "+f"(d1)
+      : "r"(a0), "r"(a1), "f"(s));
+}
+
+#define FMA32(dst, r, s)                                                              \
+  _Pragma("unroll") for (int i_ = 0; i_ < 32; i_ += 2)                                \
+      fma2((dst)[i_], (dst)[i_ + 1], (r)[i_], (r)[i_ + 1], (s))
 
 
 // ------------------------------------------------------------------ schedule
@@ -304,6 +317,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // Everything above touches only this CTA's shared memory and TMEM; from
+  // here on global memory written by the previous kernels is read.
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  pdl_wait();
+  pdl_launch_dependents();
   if (W13 && p.zero_counters != nullptr) {
     for (int i = blockIdx.x * NUM_THREADS + tid; i < p.n_zero_counters;
          i += gridDim.x * NUM_THREADS)
@@ -342,8 +363,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
       // ---------------------------------------------------------------- TMA
       if (lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_phase = 0;
@@ -569,7 +588,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         amax = fmaxf(amax, xamax[(tp * 2 + (h ^ 1)) * BM + row_local]);
         tp ^= 1;
         const uint32_t code = ue8m0_exponent(amax);
-        const float inv = __frcp_rn(__uint_as_float(code << 23));
+        const float inv = ue8m0_inverse(code);
         if (row_ok) {
           uint8_t* dst = p.y_q + grow * (int64_t)p.N + n0;
 #pragma unroll
@@ -832,8 +851,8 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
       return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the w13 operands");
     const int64_t units = mt_cap * p.n_tiles;
     const int grid = (int)(units < sms ? (units < 1 ? 1 : units) : sms);
-    moe::grouped_gemm_kernel<true><<<grid, moe::NUM_THREADS, smem, s>>>(p, tA, tB);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(moe::grouped_gemm_kernel<true>, dim3(grid), dim3(moe::NUM_THREADS),
+                               smem, s, p, tA, tB);
     if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "w13 launch: %s", cudaGetErrorString(e));
   }
   if (stages & MOE_STAGE_W2) {
@@ -862,8 +881,8 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
       return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the w2 operands");
     const int64_t units = mt_cap * nt2 * S;
     const int grid = (int)(units < sms ? (units < 1 ? 1 : units) : sms);
-    moe::grouped_gemm_kernel<false><<<grid, moe::NUM_THREADS, smem, s>>>(p, tA, tB);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(moe::grouped_gemm_kernel<false>, dim3(grid), dim3(moe::NUM_THREADS),
+                               smem, s, p, tA, tB);
     if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "w2 launch: %s", cudaGetErrorString(e));
   }
   return MOE_OK;

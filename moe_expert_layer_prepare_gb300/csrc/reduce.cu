@@ -28,11 +28,15 @@ __global__ void __launch_bounds__(256) topk_reduce_kernel(ReduceParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t chunks = (p.K + 255) / 256;
-  const int64_t tasks = p.T * chunks;
-  for (int64_t task = gwarp; task < tasks; task += nwarps) {
-    const int64_t t = task / chunks;
-    const int64_t c0 = (task - t * chunks) * 256 + lane * 8;
+  // tasks index (token, 256-column chunk) pairs; the host keeps T * chunks < 2^31
+  const uint32_t chunks = (uint32_t)((p.K + 255) / 256);
+  const uint32_t tasks = (uint32_t)(p.T * chunks);
+  pdl_wait();
+  pdl_launch_dependents();
+  for (uint32_t task = (uint32_t)gwarp; task < tasks; task += (uint32_t)nwarps) {
+    const uint32_t tq = task / chunks;
+    const int64_t t = tq;
+    const int64_t c0 = (int64_t)(task - tq * chunks) * 256 + lane * 8;
     const bool active = c0 < p.K;
     float acc[8];
 #pragma unroll
@@ -74,11 +78,11 @@ moe_status_t launch_topk_reduce(const void* expert_out, int64_t E, int64_t M_max
                       top_k, static_cast<uint16_t*>(out)};
   const int64_t tasks = T * ((K + 255) / 256);
   int64_t blocks = (tasks * 32 + 255) / 256;
-  const int64_t cap = (int64_t)num_sms() * 8;
+  const int64_t cap =
+      (int64_t)num_sms() * resident_blocks(reinterpret_cast<const void*>(moe::topk_reduce_kernel), 256);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  moe::topk_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(moe::topk_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p);
   if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "reduce launch: %s", cudaGetErrorString(e));
   return MOE_OK;
 }

@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(1024) route_kernel(StageParams p) {
   const int E = (int)p.E;
 
   for (int i = tid; i < 32 * E; i += 1024) warp_cnt[i] = 0;
+  pdl_wait();
+  pdl_launch_dependents();
 
   bool record_on;
   int64_t unpadded;
@@ -213,7 +215,7 @@ __device__ __forceinline__ uint2 quant8(const float f[8], float amax, uint32_t& 
   float inv;
   if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
     code = ue8m0_exponent(amax);
-    inv = __frcp_rn(__uint_as_float(code << 23));
+    inv = ue8m0_inverse(code);
   } else {
     const float s = __fdiv_rn(fmaxf(amax, 1.0e-4f), 448.0f);
     code = __float_as_uint(s);
@@ -231,11 +233,80 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
   asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// One task after its two loads have landed.
+template <int SF_MODE, bool DISPATCH>
+__device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int64_t w, uint4 vA,
+                                           uint4 vB, int lane) {
+  const int half = lane >> 4;
+  const int64_t gA = 4 * w + half, gB = 4 * w + 2 + half;
+  const bool actA = gA < p.G, actB = gB < p.G;
+  const int64_t e0 = 4 * w * kGroup;
+  const int64_t offA = e0 + lane * 8, offB = e0 + 256 + lane * 8;
+  if constexpr (SF_MODE == MOE_SF_NONE) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.x) + t * p.xs0;
+    if (actA) st_v4(dst + offA, vA);
+    if (actB) st_v4(dst + offB, vB);
+  } else {
+    float fA[8], fB[8];
+    const float mA = amax8(vA, fA);
+    const float mB = amax8(vB, fB);
+    uint32_t cA, cB;
+    const uint2 qA = quant8<SF_MODE>(fA, mA, cA);
+    const uint2 qB = quant8<SF_MODE>(fB, mB, cB);
+    uint8_t* xrow = p.x + t * p.xs0;
+    if (actA) st_v2(xrow + offA, qA);
+    if (actB) st_v2(xrow + offB, qB);
+
+    uint32_t word = 0;
+    if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
+      const uint32_t a = actA ? cA : 0u, b = actB ? cB : 0u;
+      const uint32_t e0w = __shfl_sync(0xFFFFFFFFu, a, 0);
+      const uint32_t e1w = __shfl_sync(0xFFFFFFFFu, a, 16);
+      const uint32_t e2w = __shfl_sync(0xFFFFFFFFu, b, 0);
+      const uint32_t e3w = __shfl_sync(0xFFFFFFFFu, b, 16);
+      word = e0w | (e1w << 8) | (e2w << 16) | (e3w << 24);
+      if (lane == 0) reinterpret_cast<uint32_t*>(p.x_sf)[t * p.sfs0 + w * p.sfs1] = word;
+    } else {
+      if ((lane & 15) == 0) {
+        float* sf = reinterpret_cast<float*>(p.x_sf) + t * p.sfs0;
+        if (actA) sf[gA * p.sfs1] = __uint_as_float(cA);
+        if (actB) sf[gB * p.sfs1] = __uint_as_float(cB);
+      }
+    }
+
+    if constexpr (DISPATCH) {
+      const int64_t K = p.K;
+      for (int64_t j = 0; j < p.top_k; ++j) {
+        const int64_t r = t * p.top_k + j;
+        const int64_t e = p.ids_out[t * p.ios0 + j * p.ios1];
+        int64_t slot = -1;
+        if (e >= 0 && e < p.E) {
+          slot = (int64_t)__ldcg(&p.hist[(r >> 10) * p.E + e]) + p.local_rank[r];
+          if (slot >= p.M_max) slot = -1;
+        }
+        if (slot >= 0) {
+          uint8_t* brow = p.x_b + (e * p.M_max + slot) * K;
+          if (actA) st_v2(brow + offA, qA);
+          if (actB) st_v2(brow + offB, qB);
+          if (lane == 0) p.sf_b[(e * p.M_max + slot) * p.W + w] = (int32_t)word;
+        }
+        if (w == 0 && lane == 0) p.route_slot[r] = (int32_t)slot;
+      }
+    }
+  }
+}
+
+// Each warp keeps the loads of QUANT_BATCH tasks (4 KB) in flight before it
+// quantises them.
+constexpr int QUANT_BATCH = 4;
+
 template <int SF_MODE, bool REPACK, bool DISPATCH, typename IdT, typename WT>
 __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
 
   if constexpr (REPACK) {
     bool record_on;
@@ -247,73 +318,30 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
       repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
   }
 
-  const int half = lane >> 4;  // group within each load
-  const int64_t tasks = p.T * p.W;
-  for (int64_t task = gwarp; task < tasks; task += nwarps) {
-    const int64_t t = task / p.W;
-    const int64_t w = task - t * p.W;
-    const int64_t gA = 4 * w + half;      // group of load A
-    const int64_t gB = 4 * w + 2 + half;  // group of load B
-    const bool actA = gA < p.G, actB = gB < p.G;
-    const int64_t e0 = 4 * w * kGroup;    // first element of the task
-    const int64_t offA = e0 + lane * 8, offB = e0 + 256 + lane * 8;
-    const uint16_t* src = p.hidden + t * p.hs0;
-    uint4 vA = make_uint4(0, 0, 0, 0), vB = vA;
-    if (actA) vA = ld_stream_v4(src + offA);
-    if (actB) vB = ld_stream_v4(src + offB);
-    if constexpr (SF_MODE == MOE_SF_NONE) {
-      uint16_t* dst = reinterpret_cast<uint16_t*>(p.x) + t * p.xs0;
-      if (actA) st_v4(dst + offA, vA);
-      if (actB) st_v4(dst + offB, vB);
-      continue;
-    } else {
-      float fA[8], fB[8];
-      const float mA = amax8(vA, fA);
-      const float mB = amax8(vB, fB);
-      uint32_t cA, cB;
-      const uint2 qA = quant8<SF_MODE>(fA, mA, cA);
-      const uint2 qB = quant8<SF_MODE>(fB, mB, cB);
-      uint8_t* xrow = p.x + t * p.xs0;
-      if (actA) st_v2(xrow + offA, qA);
-      if (actB) st_v2(xrow + offB, qB);
-
-      uint32_t word = 0;
-      if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
-        const uint32_t a = actA ? cA : 0u, b = actB ? cB : 0u;
-        const uint32_t e0w = __shfl_sync(0xFFFFFFFFu, a, 0);
-        const uint32_t e1w = __shfl_sync(0xFFFFFFFFu, a, 16);
-        const uint32_t e2w = __shfl_sync(0xFFFFFFFFu, b, 0);
-        const uint32_t e3w = __shfl_sync(0xFFFFFFFFu, b, 16);
-        word = e0w | (e1w << 8) | (e2w << 16) | (e3w << 24);
-        if (lane == 0)
-          reinterpret_cast<uint32_t*>(p.x_sf)[t * p.sfs0 + w * p.sfs1] = word;
-      } else {
-        if ((lane & 15) == 0) {
-          float* sf = reinterpret_cast<float*>(p.x_sf) + t * p.sfs0;
-          if (actA) sf[gA * p.sfs1] = __uint_as_float(cA);
-          if (actB) sf[gB * p.sfs1] = __uint_as_float(cB);
-        }
+  // tasks index (token, word) pairs; the host guarantees T * W < 2^31
+  const int half = lane >> 4;
+  const uint32_t tasks = (uint32_t)(p.T * p.W);
+  const uint32_t Wd = (uint32_t)p.W;
+  const uint32_t nw = (uint32_t)nwarps;
+  for (uint32_t base = (uint32_t)gwarp; base < tasks; base += QUANT_BATCH * nw) {
+    uint4 vA[QUANT_BATCH], vB[QUANT_BATCH];
+    uint32_t tt[QUANT_BATCH], ww[QUANT_BATCH];
+#pragma unroll
+    for (int b = 0; b < QUANT_BATCH; ++b) {
+      const uint32_t task = base + b * nw;
+      tt[b] = task / Wd;
+      ww[b] = task - tt[b] * Wd;
+      vA[b] = make_uint4(0, 0, 0, 0);
+      vB[b] = vA[b];
+      if (task < tasks) {
+        const uint16_t* src = p.hidden + (int64_t)tt[b] * p.hs0 + 4 * ww[b] * kGroup + lane * 8;
+        if (4 * ww[b] + half < p.G) vA[b] = ld_stream_v4(src);
+        if (4 * ww[b] + 2 + half < p.G) vB[b] = ld_stream_v4(src + 256);
       }
-
-      if constexpr (DISPATCH) {
-        const int64_t K = p.K;
-        for (int64_t j = 0; j < p.top_k; ++j) {
-          const int64_t r = t * p.top_k + j;
-          const int64_t e = p.ids_out[t * p.ios0 + j * p.ios1];
-          int64_t slot = -1;
-          if (e >= 0 && e < p.E) {
-            slot = (int64_t)__ldcg(&p.hist[(r >> 10) * p.E + e]) + p.local_rank[r];
-            if (slot >= p.M_max) slot = -1;
-          }
-          if (slot >= 0) {
-            uint8_t* brow = p.x_b + (e * p.M_max + slot) * K;
-            if (actA) st_v2(brow + offA, qA);
-            if (actB) st_v2(brow + offB, qB);
-            if (lane == 0) p.sf_b[(e * p.M_max + slot) * p.W + w] = (int32_t)word;
-          }
-          if (w == 0 && lane == 0) p.route_slot[r] = (int32_t)slot;
-        }
-      }
+    }
+#pragma unroll
+    for (int b = 0; b < QUANT_BATCH; ++b) {
+      if (base + b * nw < tasks) quant_task<SF_MODE, DISPATCH>(p, tt[b], ww[b], vA[b], vB[b], lane);
     }
   }
 }
@@ -336,15 +364,19 @@ size_t prepare_workspace_size(int64_t T, int64_t k, int64_t E) {
   return bytes;
 }
 
+template <typename Kernel>
+static int64_t quant_grid(Kernel k, int64_t tasks) {
+  // one wave of resident blocks: every warp loops over its share of tasks
+  int64_t blocks = (tasks * 32 + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * resident_blocks(reinterpret_cast<const void*>(k), 256);
+  if (blocks > cap) blocks = cap;
+  return blocks < 1 ? 1 : blocks;
+}
+
 template <typename IdT, typename WT>
 static moe_status_t launch_typed(StageParams& p, bool dispatch, int sf_mode, cudaStream_t s) {
-  const int sms = num_sms();
   const int64_t tasks = p.T * p.W;
   const int threads = 256;
-  int64_t blocks = (tasks * 32 + threads - 1) / threads;
-  const int64_t cap = (int64_t)sms * 8;  // 8 resident blocks of 256 threads per SM
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
   if (dispatch) {
     const int64_t R = p.T * p.top_k;
     const int64_t B = (R + 1023) / 1024;
@@ -359,21 +391,30 @@ static moe_status_t launch_typed(StageParams& p, bool dispatch, int sf_mode, cud
     }
     cudaError_t e = cudaMemsetAsync(p.done, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
-    rk<<<(unsigned)B, 1024, smem, s>>>(p);
-    moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT>
-        <<<(unsigned)blocks, threads, 0, s>>>(p);
+    cudaError_t le = launch_pdl(rk, dim3((unsigned)B), dim3(1024), smem, s, p);
+    if (le != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "route_kernel launch: %s", cudaGetErrorString(le));
+    auto qk = moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT>;
+    le = launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+    if (le != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "quant_kernel launch: %s", cudaGetErrorString(le));
   } else {
     switch (sf_mode) {
-      case MOE_SF_NONE:
-        moe::quant_kernel<MOE_SF_NONE, true, false, IdT, WT><<<(unsigned)blocks, threads, 0, s>>>(p);
+      case MOE_SF_NONE: {
+        auto qk = moe::quant_kernel<MOE_SF_NONE, true, false, IdT, WT>;
+        launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
         break;
-      case MOE_SF_UE8M0_PACKED:
-        moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT>
-            <<<(unsigned)blocks, threads, 0, s>>>(p);
+      }
+      case MOE_SF_UE8M0_PACKED: {
+        auto qk = moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT>;
+        launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
         break;
-      default:
-        moe::quant_kernel<MOE_SF_FP32, true, false, IdT, WT><<<(unsigned)blocks, threads, 0, s>>>(p);
+      }
+      default: {
+        auto qk = moe::quant_kernel<MOE_SF_FP32, true, false, IdT, WT>;
+        launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
         break;
+      }
     }
   }
   cudaError_t e = cudaGetLastError();

@@ -46,6 +46,11 @@ CONFIGS = {
                             zipf_s=1.1, padding_frac=0.02),
     "deepseek_prefill": dict(index=4, T=8192, K=7168, N=2048, E=256, top_k=8, M_max=1024,
                              zipf_s=None, padding_frac=0.0),
+    # profiling stand-in for deepseek_prefill: the same per-expert load
+    # (~256 rows per expert) and shapes over 32 experts, small enough for a
+    # full counter capture
+    "deepseek_prefill_e32": dict(index=6, T=1024, K=7168, N=2048, E=32, top_k=8, M_max=1024,
+                                 zipf_s=None, padding_frac=0.0),
     "staging_stress": dict(index=5, T=16384, K=7168, N=None, E=256, top_k=8, M_max=None,
                            zipf_s=None, padding_frac=0.0, outlier_frac=0.01,
                            outlier_scale=50.0, zero_group_frac=0.005,
