@@ -153,6 +153,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// One lane of the (converged) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile("{ .reg .pred p; elect.sync _|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -220,23 +227,10 @@ __device__ __forceinline__ void tmem_wait_ld() {
                :                                                                                \
                : "memory")
 
-// dst[i] += r[i] * s for 32 columns, two lanes per instruction (paired fp32
-// FMA, round-to-nearest like fmaf).
-__device__ __forceinline__ void fma2(float& d0, float& d1, uint32_t a0, uint32_t a1, float s) {
-  asm("{ .reg .b64 a, b, c;\n\t"
-      "mov.b64 a, {%2, %3};\n\t"
-      "mov.b64 b, {%4, %4};\n\t"
-      "mov.b64 c, {%0, %1};\n\t"
-      "fma.rn.f32x2 c, a, b, c;\n\t"
-      "mov.b64 {%0, %1}, c; }"
-      : "+f"(d0), "+f"(d1)
-      : "r"(a0), "r"(a1), "f"(s));
-}
-
-#define FMA32(dst, r, s)                                                              \
-  _Pragma("unroll") for (int i_ = 0; i_ < 32; i_ += 2)                                \
-      fma2((dst)[i_], (dst)[i_ + 1], (r)[i_], (r)[i_ + 1], (s))
-
+// dst[i] += r[i] * s for 32 columns (fp32, round to nearest).
+#define FMA32(dst, r, s)                                        \
+  _Pragma("unroll") for (int i_ = 0; i_ < 32; ++i_) (dst)[i_] = \
+      fmaf(__uint_as_float((r)[i_]), (s), (dst)[i_])
 
 // ------------------------------------------------------------------ schedule
 struct Unit {
@@ -360,97 +354,107 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp < EPI_WARP0) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PRODUCER_REGS));
+    // The producer and MMA loops run on all 32 lanes of their warp with
+    // warp-uniform control flow, so every tcgen05 / TMA operand stays
+    // warp-uniform; one elected lane issues each instruction.
     if (warp == 0) {
       // ---------------------------------------------------------------- TMA
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t issued_mask = 0, issued_phase = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-          const Unit w = decode_unit(p, prefix, u, cnt);
-          const int a_row0 = w.e * p.M_max + w.mt * BM;
-          const int n_boxes = (w.rows + A_BOX_ROWS - 1) / A_BOX_ROWS;
-          const uint32_t tx = (uint32_t)(n_boxes * A_BOX_ROWS * BK + B_BYTES);
-          int b_row0, b_row1;
-          if constexpr (W13) {
-            b_row0 = w.e * p.b_rows + w.nt * 128;
-            b_row1 = w.e * p.b_rows + p.N + w.nt * 128;
-          } else {
-            b_row0 = w.e * p.b_rows + w.nt * 256;
-            b_row1 = b_row0 + 128;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit w = decode_unit(p, prefix, u, cnt);
+        const int a_row0 = w.e * p.M_max + w.mt * BM;
+        const int n_boxes = (w.rows + A_BOX_ROWS - 1) / A_BOX_ROWS;
+        const uint32_t tx = (uint32_t)(n_boxes * A_BOX_ROWS * BK + B_BYTES);
+        int b_row0, b_row1;
+        if constexpr (W13) {
+          b_row0 = w.e * p.b_rows + w.nt * 128;
+          b_row1 = w.e * p.b_rows + p.N + w.nt * 128;
+        } else {
+          b_row0 = w.e * p.b_rows + w.nt * 256;
+          b_row1 = b_row0 + 128;
+        }
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status))) {
+            ok = false;
+            break;
           }
-          for (int kb = w.kb0; kb < w.kb1; ++kb) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            const uint32_t fb = full0 + 8 * stage;
+          const uint32_t fb = full0 + 8 * stage;
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          if (elect_one()) {
             mbar_expect_tx(fb, tx);
-            const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-            const uint32_t sb = sa + A_BYTES;
             for (int i = 0; i < n_boxes; ++i)
               tma_load_2d(sa + i * A_BOX_ROWS * BK, &tmA, kb * BK, a_row0 + i * A_BOX_ROWS, fb);
             tma_load_2d(sb, &tmB, kb * BK, b_row0, fb);
             tma_load_2d(sb + 128 * BK, &tmB, kb * BK, b_row1, fb);
-            issued_mask |= 1u << stage;
-            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
           }
-        }
-        // Drain: every issued stage's copy must have landed before exit.
-        for (int s = 0; s < STAGES; ++s) {
-          if (issued_mask & (1u << s)) {
-            volatile int never = 0;
-            mbar_wait(full0 + 8 * s, (issued_phase >> s) & 1u, &never, p.status);
+          __syncwarp();
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
       }
+      // Drain: every issued stage's copy must have landed before exit.
+      for (int st = 0; st < STAGES; ++st) {
+        if (issued_mask & (1u << st)) {
+          volatile int never = 0;
+          mbar_wait(full0 + 8 * st, (issued_phase >> st) & 1u, &never, p.status);
+        }
+      }
+      __syncwarp();
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        int ab = 0;
-        uint32_t aphase = 0;
-        bool ok = true;
-        bool any = false;
-        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-          const Unit w = decode_unit(p, prefix, u, cnt);
-          for (int kb = w.kb0; kb < w.kb1; ++kb) {
-            if (!mbar_wait(tempty0 + 8 * ab, aphase ^ 1u, abort_flag, p.status) ||
-                !mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-            const uint64_t adesc = sw128_desc(sa);
-            const uint64_t bdesc = sw128_desc(sa + A_BYTES);
-            const uint32_t d = tmem_base + (uint32_t)(ab * BN);
-  #pragma unroll
+      int stage = 0;
+      uint32_t phase = 0;
+      int ab = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      bool any = false;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit w = decode_unit(p, prefix, u, cnt);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          const bool ready = mbar_wait(tempty0 + 8 * ab, aphase ^ 1u, abort_flag, p.status) &&
+                             mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status);
+          if (!__all_sync(0xFFFFFFFFu, ready)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t adesc = sw128_desc(sa);
+          const uint64_t bdesc = sw128_desc(sa + A_BYTES);
+          const uint32_t d = tmem_base + (uint32_t)(ab * BN);
+          if (elect_one()) {
+#pragma unroll
             for (int k = 0; k < BK / 32; ++k)
               mma_f8(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), k > 0 ? 1u : 0u);
             mma_commit(empty0 + 8 * stage);
             mma_commit(tfull0 + 8 * ab);
-            any = true;
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-            ab ^= 1;
-            if (ab == 0) aphase ^= 1u;
           }
+          __syncwarp();
+          any = true;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          ab ^= 1;
+          if (ab == 0) aphase ^= 1u;
         }
-        if (any) {
-          // all MMAs of this CTA complete before TMEM is freed
-          mma_commit(mma_done);
-          volatile int never = 0;
-          mbar_wait(mma_done, 0, &never, p.status);
-        }
+      }
+      if (any) {
+        // all MMAs of this CTA complete before TMEM is freed
+        if (elect_one()) mma_commit(mma_done);
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(mma_done, 0, &never, p.status);
+        __syncwarp();
       }
     }
   } else {

@@ -296,9 +296,32 @@ __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int6
   }
 }
 
-// Each warp keeps the loads of QUANT_BATCH tasks (4 KB) in flight before it
-// quantises them.
+// Each warp keeps the loads of QUANT_BATCH tasks (4 KB) in flight, and issues
+// the loads of its next batch before it quantises the current one.
 constexpr int QUANT_BATCH = 4;
+
+struct TaskBatch {
+  uint4 vA[QUANT_BATCH], vB[QUANT_BATCH];
+  uint32_t t[QUANT_BATCH], w[QUANT_BATCH];
+};
+
+__device__ __forceinline__ void load_batch(const StageParams& p, TaskBatch& b, uint32_t base,
+                                           uint32_t nw, uint32_t tasks, uint32_t Wd, int lane) {
+  const int half = lane >> 4;
+#pragma unroll
+  for (int i = 0; i < QUANT_BATCH; ++i) {
+    const uint32_t task = base + i * nw;
+    b.t[i] = task / Wd;
+    b.w[i] = task - b.t[i] * Wd;
+    b.vA[i] = make_uint4(0, 0, 0, 0);
+    b.vB[i] = b.vA[i];
+    if (task < tasks) {
+      const uint16_t* src = p.hidden + (int64_t)b.t[i] * p.hs0 + 4 * b.w[i] * kGroup + lane * 8;
+      if (4 * b.w[i] + half < p.G) b.vA[i] = ld_stream_v4(src);
+      if (4 * b.w[i] + 2 + half < p.G) b.vB[i] = ld_stream_v4(src + 256);
+    }
+  }
+}
 
 template <int SF_MODE, bool REPACK, bool DISPATCH, typename IdT, typename WT>
 __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
@@ -308,6 +331,27 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
   pdl_wait();
   pdl_launch_dependents();
 
+  // tasks index (token, word) pairs; the host guarantees T * W < 2^31
+  const uint32_t tasks = (uint32_t)(p.T * p.W);
+  const uint32_t Wd = (uint32_t)p.W;
+  const uint32_t nw = (uint32_t)nwarps;
+  const uint32_t step = QUANT_BATCH * nw;
+  uint32_t base = (uint32_t)gwarp;
+  TaskBatch cur, nxt;
+  if (base < tasks) load_batch(p, cur, base, nw, tasks, Wd, lane);
+  for (; base < tasks; base += step) {
+    const bool more = base + step < tasks;
+    if (more) load_batch(p, nxt, base + step, nw, tasks, Wd, lane);
+#pragma unroll
+    for (int i = 0; i < QUANT_BATCH; ++i) {
+      if (base + i * nw < tasks)
+        quant_task<SF_MODE, DISPATCH>(p, cur.t[i], cur.w[i], cur.vA[i], cur.vB[i], lane);
+    }
+    if (more) cur = nxt;
+  }
+
+  // The top-k repack (dependent loads, no bandwidth) goes last so that its
+  // latency overlaps the other warps' streaming.
   if constexpr (REPACK) {
     bool record_on;
     int64_t unpadded;
@@ -316,33 +360,6 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
     for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R;
          r += (int64_t)gridDim.x * blockDim.x)
       repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
-  }
-
-  // tasks index (token, word) pairs; the host guarantees T * W < 2^31
-  const int half = lane >> 4;
-  const uint32_t tasks = (uint32_t)(p.T * p.W);
-  const uint32_t Wd = (uint32_t)p.W;
-  const uint32_t nw = (uint32_t)nwarps;
-  for (uint32_t base = (uint32_t)gwarp; base < tasks; base += QUANT_BATCH * nw) {
-    uint4 vA[QUANT_BATCH], vB[QUANT_BATCH];
-    uint32_t tt[QUANT_BATCH], ww[QUANT_BATCH];
-#pragma unroll
-    for (int b = 0; b < QUANT_BATCH; ++b) {
-      const uint32_t task = base + b * nw;
-      tt[b] = task / Wd;
-      ww[b] = task - tt[b] * Wd;
-      vA[b] = make_uint4(0, 0, 0, 0);
-      vB[b] = vA[b];
-      if (task < tasks) {
-        const uint16_t* src = p.hidden + (int64_t)tt[b] * p.hs0 + 4 * ww[b] * kGroup + lane * 8;
-        if (4 * ww[b] + half < p.G) vA[b] = ld_stream_v4(src);
-        if (4 * ww[b] + 2 + half < p.G) vB[b] = ld_stream_v4(src + 256);
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < QUANT_BATCH; ++b) {
-      if (base + b * nw < tasks) quant_task<SF_MODE, DISPATCH>(p, tt[b], ww[b], vA[b], vB[b], lane);
-    }
   }
 }
 
