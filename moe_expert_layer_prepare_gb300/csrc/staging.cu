@@ -69,7 +69,8 @@ struct StageParams {
 // load record.  Returns the id written.
 template <typename IdT, typename WT>
 __device__ __forceinline__ int64_t repack_route(const StageParams& p, int64_t t, int64_t j,
-                                                bool record_on, int64_t unpadded) {
+                                                bool record_on, int64_t unpadded,
+                                                int* smem_load = nullptr) {
   bool is_pad = p.pad ? (p.pad[t * p.ps0] != 0) : false;
   int64_t id = (int64_t)(reinterpret_cast<const IdT*>(p.ids)[t * p.is0 + j * p.is1]);
   float w;
@@ -98,7 +99,12 @@ __device__ __forceinline__ int64_t repack_route(const StageParams& p, int64_t t,
           id = -1;
         } else {
           id = phys;
-          if (p.load != nullptr && record_on && t < unpadded) atomicAdd(&p.load[phys], 1);
+          if (p.load != nullptr && record_on && t < unpadded) {
+            if (smem_load != nullptr)
+              atomicAdd(&smem_load[phys], 1);
+            else
+              atomicAdd(&p.load[phys], 1);
+          }
         }
       }
     }
@@ -296,6 +302,11 @@ __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int6
   }
 }
 
+// Shared-memory load histogram of the repack (physical experts) and the number
+// of blocks that share the recorded routes.
+constexpr int kLoadBins = 2048;
+constexpr int kLoadBlocks = 24;
+
 // Each warp keeps the loads of QUANT_BATCH tasks (4 KB) in flight, and issues
 // the loads of its next batch before it quantises the current one.
 constexpr int QUANT_BATCH = 4;
@@ -323,13 +334,50 @@ __device__ __forceinline__ void load_batch(const StageParams& p, TaskBatch& b, u
   }
 }
 
+// Repack of routes [r0, r1) with the EPLB load counted in a shared-memory
+// histogram that is added to the global counters once per non-zero bin.
+// Per-route global atomics would land on the few L2 lines that hold the
+// counters and serialise there.
+template <typename IdT, typename WT>
+__device__ __forceinline__ void repack_recorded(const StageParams& p, int64_t r0, int64_t r1,
+                                                int64_t unpadded, int* s_load) {
+  for (int i = threadIdx.x; i < p.num_physical; i += blockDim.x) s_load[i] = 0;
+  __syncthreads();
+  for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x)
+    repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, true, unpadded, s_load);
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.num_physical; i += blockDim.x)
+    if (s_load[i] != 0) atomicAdd(&p.load[i], s_load[i]);
+}
+
 template <int SF_MODE, bool REPACK, bool DISPATCH, typename IdT, typename WT>
 __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
+  __shared__ int s_load[REPACK ? kLoadBins : 1];
   const int lane = threadIdx.x & 31;
-  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   pdl_wait();
   pdl_launch_dependents();
+
+  bool record_on = false;
+  int64_t unpadded = p.T;
+  if constexpr (REPACK) record_flags(p, record_on, unpadded);
+  const int64_t R = p.T * p.top_k;
+  // With load recording on, the repack runs in a few blocks of its own that
+  // take contiguous route ranges; when the grid is large enough they are
+  // set aside from the streaming so that their dependent-load chains overlap
+  // it instead of trailing it.
+  const bool recorded = REPACK && record_on && p.load != nullptr && p.num_physical <= kLoadBins;
+  const int64_t nrep = recorded ? min((int64_t)gridDim.x, (int64_t)kLoadBlocks) : 0;
+  const bool set_aside = recorded && gridDim.x >= 4 * kLoadBlocks;
+  if (set_aside && blockIdx.x < nrep) {
+    const int64_t per = (R + nrep - 1) / nrep;
+    repack_recorded<IdT, WT>(p, blockIdx.x * per, min(R, (blockIdx.x + 1) * per), unpadded,
+                             s_load);
+    return;
+  }
+  const int64_t sblock = set_aside ? blockIdx.x - nrep : blockIdx.x;
+  const int64_t sgrid = set_aside ? gridDim.x - nrep : gridDim.x;
+  const int64_t gwarp = (sblock * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (sgrid * blockDim.x) >> 5;
 
   // tasks index (token, word) pairs; the host guarantees T * W < 2^31
   const uint32_t tasks = (uint32_t)(p.T * p.W);
@@ -350,16 +398,21 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
     if (more) cur = nxt;
   }
 
-  // The top-k repack (dependent loads, no bandwidth) goes last so that its
-  // latency overlaps the other warps' streaming.
+  // Without recording (or on a small grid) the top-k repack (dependent
+  // loads, no bandwidth) goes last so that its latency overlaps the other
+  // warps' streaming.
   if constexpr (REPACK) {
-    bool record_on;
-    int64_t unpadded;
-    record_flags(p, record_on, unpadded);
-    const int64_t R = p.T * p.top_k;
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R;
-         r += (int64_t)gridDim.x * blockDim.x)
-      repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
+    if (recorded) {
+      if (!set_aside && blockIdx.x < nrep) {
+        const int64_t per = (R + nrep - 1) / nrep;
+        repack_recorded<IdT, WT>(p, blockIdx.x * per, min(R, (blockIdx.x + 1) * per), unpadded,
+                                 s_load);
+      }
+    } else {
+      for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R;
+           r += (int64_t)gridDim.x * blockDim.x)
+        repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
+    }
   }
 }
 
