@@ -507,19 +507,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
 
-      // scales of the slab, loaded one slab ahead
+      // Scales of the slabs, fetched ahead of use: under the GEMM's L2
+      // traffic a scale load takes about as long as a slab.  The weight block
+      // scales are the same for every row, so lane i holds slab i of a
+      // 32-slab window (the next window is fetched a window ahead) and each
+      // slab takes its pair by shuffle; the packed activation exponents of
+      // the row run one 4-slab word ahead.
+      int wb = w.kb0;
+      float wg_cur = wb + lane < w.kb1 ? __ldg(ws0 + wb + lane) : 0.0f;
+      float wu_cur = wb + lane < w.kb1 ? __ldg(ws1 + wb + lane) : 0.0f;
+      float wg_nxt = wb + 32 + lane < w.kb1 ? __ldg(ws0 + wb + 32 + lane) : 0.0f;
+      float wu_nxt = wb + 32 + lane < w.kb1 ? __ldg(ws1 + wb + 32 + lane) : 0.0f;
       uint32_t aw = row_ok ? __ldg(asf_row + (w.kb0 >> 2)) : 0x7F7F7F7Fu;
-      float wsc0 = __ldg(ws0 + w.kb0), wsc1 = __ldg(ws1 + w.kb0);
+      uint32_t aw_next = (row_ok && ((w.kb0 >> 2) + 1) * 4 < w.kb1)
+                             ? __ldg(asf_row + (w.kb0 >> 2) + 1) : 0x7F7F7F7Fu;
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        if (kb > w.kb0 && (kb & 3) == 0) {
+          aw = aw_next;
+          if (row_ok && ((kb >> 2) + 1) * 4 < w.kb1) aw_next = __ldg(asf_row + (kb >> 2) + 1);
+        }
+        if (kb - wb == 32) {
+          wb = kb;
+          wg_cur = wg_nxt;
+          wu_cur = wu_nxt;
+          wg_nxt = wb + 32 + lane < w.kb1 ? __ldg(ws0 + wb + 32 + lane) : 0.0f;
+          wu_nxt = wb + 32 + lane < w.kb1 ? __ldg(ws1 + wb + 32 + lane) : 0.0f;
+        }
         const uint32_t ea = (aw >> (8 * (kb & 3))) & 0xFFu;
         const float sa = __uint_as_float(max(ea, 1u) << 23);
-        const float s0 = sa * wsc0;
-        const float s1 = sa * wsc1;
-        if (kb + 1 < w.kb1) {
-          if (((kb + 1) & 3) == 0 && row_ok) aw = __ldg(asf_row + ((kb + 1) >> 2));
-          wsc0 = __ldg(ws0 + kb + 1);
-          wsc1 = __ldg(ws1 + kb + 1);
-        }
+        const float s0 = sa * __shfl_sync(0xFFFFFFFFu, wg_cur, kb - wb);
+        const float s1 = sa * __shfl_sync(0xFFFFFFFFu, wu_cur, kb - wb);
         // warp-uniform outcome; also reconverges the warp before the
         // .sync.aligned TMEM loads
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * ab, aphase, abort_flag, p.status))) {
