@@ -210,6 +210,43 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         "=r"(r[31])                                                                           \
       : "r"(taddr))
 
+// 64 consecutive TMEM columns of this warp's 32 lanes into 64 registers.
+#define TMEM_LD64(taddr, r)                                                              \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {"                                \
+               "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,"                \
+               "%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,"                \
+               "%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"             \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), \
+                 "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), \
+                 "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), \
+                 "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), \
+                 "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), \
+                 "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), \
+                 "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), \
+                 "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), \
+                 "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), \
+                 "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), \
+                 "=r"(r[61]), "=r"(r[62]), "=r"(r[63]) \
+               : "r"(taddr))
+
+// Wait for outstanding TMEM loads; the 64 destination registers are tied to
+// the wait so that no use of them is scheduled before it.
+#define TMEM_WAIT_PIN64(r)                                                               \
+  asm volatile("tcgen05.wait::ld.sync.aligned;"                                         \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), \
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), \
+                 "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), \
+                 "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), \
+                 "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), \
+                 "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), \
+                 "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), \
+                 "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), \
+                 "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), \
+                 "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), \
+                 "+r"(r[61]), "+r"(r[62]), "+r"(r[63]) \
+               :                                                                        \
+               : "memory")
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -546,23 +583,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (warp_active) {
           tc_fence_after();
           const uint32_t base = lane_addr + (uint32_t)(ab * BN);
-          uint32_t ra[32], rb[32];
-          // ping-pong: the load of one group overlaps the FMAs of the other
-          TMEM_LD32(base + cg[0], ra);
-          TMEM_WAIT_PIN32(ra);
-          TMEM_LD32(base + cg[1], rb);
-          FMA32(acc + 0, ra, s0);
-          TMEM_WAIT_PIN32(rb);
-          TMEM_LD32(base + cg[2], ra);
-          FMA32(acc + 32, rb, s0);
-          TMEM_WAIT_PIN32(ra);
-          TMEM_LD32(base + cg[3], rb);
-          FMA32(acc + 64, ra, W13 ? s1 : s0);
-          TMEM_WAIT_PIN32(rb);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
-          FMA32(acc + 96, rb, W13 ? s1 : s0);
+          if constexpr (W13) {
+            // gate and up halves: two 64-column loads, one wait each (fewer
+            // TMEM instructions and waits measured faster here)
+            uint32_t r64[64];
+            TMEM_LD64(base + cg[0], r64);
+            TMEM_WAIT_PIN64(r64);
+            FMA32(acc + 0, r64, s0);
+            FMA32(acc + 32, r64 + 32, s0);
+            TMEM_LD64(base + cg[2], r64);
+            TMEM_WAIT_PIN64(r64);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
+            FMA32(acc + 64, r64, s1);
+            FMA32(acc + 96, r64 + 32, s1);
+          } else {
+            uint32_t ra[32], rb[32];
+            // ping-pong: the load of one group overlaps the FMAs of the other
+            TMEM_LD32(base + cg[0], ra);
+            TMEM_WAIT_PIN32(ra);
+            TMEM_LD32(base + cg[1], rb);
+            FMA32(acc + 0, ra, s0);
+            TMEM_WAIT_PIN32(rb);
+            TMEM_LD32(base + cg[2], ra);
+            FMA32(acc + 32, rb, s0);
+            TMEM_WAIT_PIN32(ra);
+            TMEM_LD32(base + cg[3], rb);
+            FMA32(acc + 64, ra, s0);
+            TMEM_WAIT_PIN32(rb);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
+            FMA32(acc + 96, rb, s0);
+          }
         } else {
           // no row of this warp holds a token: nothing to read
           __syncwarp();
