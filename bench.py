@@ -316,12 +316,18 @@ def bench_ours(args, world, rank, local):
     w13_tfs = alg["w13_flops"] / (means[1] * 1e-3) / 1e12
     prefill = name == "deepseek_prefill"
     if prefill:
-        peak = peaks["bf16"] * FP8_OVER_BF16
+        # the GEMM is timed inside a step loop that runs for seconds under the
+        # power cap, so its denominator is the sustained figure (the burst one
+        # is reported beside it)
+        peak = peaks["bf16_sus"] * FP8_OVER_BF16
+        burst = peaks["bf16"] * FP8_OVER_BF16
         roof = dict(bound="tensor", achieved=round(w13_tfs, 2), peak=round(peak, 1),
                     unit="TFLOP/s", frac=round(w13_tfs / peak, 4),
                     traffic=ncu_traffic(name, "grouped_gemm_kernel<W13>"),
                     kernel="grouped_gemm_kernel<W13>",
-                    peak_source=f"{peaks['src']} bf16 burst x {FP8_OVER_BF16} (fp8/bf16 nominal)")
+                    peak_source=f"{peaks['src']} bf16 sustained x {FP8_OVER_BF16} "
+                                f"(fp8/bf16 nominal)",
+                    frac_of_burst=round(w13_tfs / burst, 4), burst_peak=round(burst, 1))
     else:
         roof = dict(bound="hbm", achieved=round(w13_gbs, 1), peak=peaks["hbm"], unit="GB/s",
                     frac=round(w13_gbs / peaks["hbm"], 4),

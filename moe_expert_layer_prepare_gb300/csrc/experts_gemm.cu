@@ -713,29 +713,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (*s_flag) {
             __threadfence();
             if (row_ok && cols_ok) {
-              float* sum = acc;  // partials are summed in split order
-#pragma unroll
-              for (int i = 0; i < 128; ++i) sum[i] = 0.0f;
-              for (int s = 0; s < p.splits; ++s) {
-                const float* src = p.partials + ((int64_t)s * EM + grow) * p.K + c0;
-#pragma unroll
-                for (int i = 0; i < 128; i += 4) {
-                  const float4 v = __ldcg(reinterpret_cast<const float4*>(src + i));
-                  sum[i] += v.x;
-                  sum[i + 1] += v.y;
-                  sum[i + 2] += v.z;
-                  sum[i + 3] += v.w;
-                }
-              }
+              // partials are summed in split order, 32 columns at a time
               uint16_t* dst = p.out + grow * (int64_t)p.K + c0;
+#pragma unroll 1
+              for (int c = 0; c < 128; c += 32) {
+                float sum[32];
 #pragma unroll
-              for (int i = 0; i < 128; i += 8) {
-                uint4 v;
-                v.x = f32_to_bf16_bits(sum[i]) | (f32_to_bf16_bits(sum[i + 1]) << 16);
-                v.y = f32_to_bf16_bits(sum[i + 2]) | (f32_to_bf16_bits(sum[i + 3]) << 16);
-                v.z = f32_to_bf16_bits(sum[i + 4]) | (f32_to_bf16_bits(sum[i + 5]) << 16);
-                v.w = f32_to_bf16_bits(sum[i + 6]) | (f32_to_bf16_bits(sum[i + 7]) << 16);
-                st_v4(dst + i, v);
+                for (int i = 0; i < 32; ++i) sum[i] = 0.0f;
+                for (int s = 0; s < p.splits; ++s) {
+                  const float* src = p.partials + ((int64_t)s * EM + grow) * p.K + c0 + c;
+#pragma unroll
+                  for (int i = 0; i < 32; i += 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + i));
+                    sum[i] += v.x;
+                    sum[i + 1] += v.y;
+                    sum[i + 2] += v.z;
+                    sum[i + 3] += v.w;
+                  }
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                  uint4 v;
+                  v.x = f32_to_bf16_bits(sum[i]) | (f32_to_bf16_bits(sum[i + 1]) << 16);
+                  v.y = f32_to_bf16_bits(sum[i + 2]) | (f32_to_bf16_bits(sum[i + 3]) << 16);
+                  v.z = f32_to_bf16_bits(sum[i + 4]) | (f32_to_bf16_bits(sum[i + 5]) << 16);
+                  v.w = f32_to_bf16_bits(sum[i + 6]) | (f32_to_bf16_bits(sum[i + 7]) << 16);
+                  st_v4(dst + c + i, v);
+                }
               }
             }
             if (tid == EPI_WARP0 * 32) *ctr = 0;
