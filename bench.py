@@ -42,9 +42,9 @@ FLUSH_BYTES = 512 << 20  # > 129 MB L2
 GEMM_SRC = "moe_expert_layer_prepare_gb300/csrc/experts_gemm.cu"
 STAGING_SRC = "moe_expert_layer_prepare_gb300/csrc/staging.cu"
 NCU_TRAFFIC = {
-    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (953.12e6, GEMM_SRC, "b31064923d0facf6"),
-    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1148.73e6, GEMM_SRC,
-                                                       "b31064923d0facf6"),
+    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (952.71e6, GEMM_SRC, "511edd3914739514"),
+    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1148.09e6, GEMM_SRC,
+                                                       "511edd3914739514"),
     ("staging_stress", "quant_kernel<UE8M0,repack>"): (296.73e6, STAGING_SRC,
                                                        "65cdc72dce59110e"),
 }
