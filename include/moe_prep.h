@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define MOE_PREP_ABI_VERSION 1
+#define MOE_PREP_ABI_VERSION 2
 
 typedef enum moe_status {
   MOE_OK = 0,
@@ -96,6 +96,20 @@ typedef enum moe_activation { MOE_ACT_SILU = 0 } moe_activation_t;
 /* when s >= max_tokens_per_expert, which also sets MOE_DEV_CAPACITY),       */
 /* expert_num_tokens[e] = min(#routes to e, max_tokens_per_expert).          */
 /*                                                                           */
+/* Shared-expert scale pages (when shared_x_sf != NULL; defined by the      */
+/* shared_x_sf / shared_block_m arguments of prepare_megamoe_inputs and by   */
+/* _shared_sf_row on the same page; requires MOE_SF_UE8M0_PACKED): the      */
+/* exponent byte e of group g of token t is also written to                  */
+/*   shared_x_sf[row(t) * shared_x_sf_stride0 + g * shared_x_sf_stride1],   */
+/* one uint8 per (row, group) (reading: the page's UE8M0 scale element is    */
+/* its exponent byte).  With B = shared_block_m, A = ceil(B/128)*128,        */
+/* b = t / B and m = t % B:                                                  */
+/*   row(t) = b*A + (m/128)*128 + (m%32)*4 + (m%128)/32,                     */
+/* i.e. each 128-row page interleaves its four 32-token quarters row by row */
+/* (the MN-major layout a tcgen05.cp of the scales expects).  Rows that no   */
+/* token maps to are left untouched.  The buffer must hold at least         */
+/* ceil(T/B)*A rows (shared_x_sf_rows), else SHAPE.                          */
+/*                                                                           */
 /* Errors: T == 0 -> MOE_OK, nothing enqueued.  K % 128 != 0 -> SHAPE.       */
 /* x_sf given iff sf_mode != NONE, else INVALID_ARGUMENT.  top_k < 1 ->       */
 /* SHAPE.  hidden / x rows must start on 16-byte boundaries (ALIGNMENT).     */
@@ -122,6 +136,10 @@ typedef struct moe_prepare_args {
   void* x_sf; /* NULL iff sf_mode == MOE_SF_NONE */
   int32_t sf_mode;
   int64_t x_sf_stride0, x_sf_stride1;
+  uint8_t* shared_x_sf;    /* nullable; UE8M0 exponent bytes [shared_x_sf_rows, K/128] */
+  int64_t shared_x_sf_stride0, shared_x_sf_stride1;
+  int64_t shared_x_sf_rows; /* rows of shared_x_sf */
+  int64_t shared_block_m;   /* > 0 iff shared_x_sf != NULL */
   int64_t* topk_idx_out; /* int64 [T, k] */
   int64_t topk_idx_out_stride0, topk_idx_out_stride1;
   float* topk_weights_out; /* fp32 [T, k] */

@@ -40,6 +40,8 @@ class PrepareArgs(ctypes.Structure):
         ("is_padding", _vp), ("is_padding_stride0", _i64),
         ("x", _vp), ("x_stride0", _i64),
         ("x_sf", _vp), ("sf_mode", _i32), ("x_sf_stride0", _i64), ("x_sf_stride1", _i64),
+        ("shared_x_sf", _vp), ("shared_x_sf_stride0", _i64), ("shared_x_sf_stride1", _i64),
+        ("shared_x_sf_rows", _i64), ("shared_block_m", _i64),
         ("topk_idx_out", _vp), ("topk_idx_out_stride0", _i64), ("topk_idx_out_stride1", _i64),
         ("topk_weights_out", _vp), ("topk_weights_out_stride0", _i64),
         ("topk_weights_out_stride1", _i64),
@@ -129,8 +131,11 @@ def experts_workspace_size(E, M_max, K, N, valid_shape_m, which) -> int:
 
 def moe_prepare_inputs(hidden, topk_ids, topk_weights, x, x_sf, topk_idx_out, topk_weights_out,
                        is_padding=None, sf_mode=MOE_SF_UE8M0_PACKED, eplb=None, dispatch=None,
-                       device_status=None, stream=None):
+                       device_status=None, stream=None, shared_x_sf=None, shared_block_m=None):
     """Input staging (and optional dispatch).  See include/moe_prep.h.
+
+    shared_x_sf: uint8 [rows, K/128] shared-expert scale pages, given together
+    with shared_block_m (UE8M0 scales only).
 
     eplb: dict(logical_to_physical, logical_replica_count, expert_load=None,
                should_record=None, num_unpadded_tokens=None) -- device tensors.
@@ -161,6 +166,12 @@ def moe_prepare_inputs(hidden, topk_ids, topk_weights, x, x_sf, topk_idx_out, to
     a.topk_weights_out = _ptr(topk_weights_out)
     a.topk_weights_out_stride0 = topk_weights_out.stride(0)
     a.topk_weights_out_stride1 = topk_weights_out.stride(1)
+    if shared_x_sf is not None:
+        a.shared_x_sf = _ptr(shared_x_sf)
+        a.shared_x_sf_stride0, a.shared_x_sf_stride1 = shared_x_sf.stride(0), shared_x_sf.stride(1)
+        a.shared_x_sf_rows = shared_x_sf.shape[0]
+    if shared_block_m is not None:
+        a.shared_block_m = int(shared_block_m)
     if eplb:
         l2p = eplb["logical_to_physical"]
         a.logical_to_physical, a.num_logical, a.map_stride = _ptr(l2p), l2p.shape[0], l2p.stride(0)

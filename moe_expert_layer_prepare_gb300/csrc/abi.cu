@@ -109,6 +109,22 @@ moe_status_t moe_prepare_inputs(const moe_prepare_args_t* a, void* stream) {
     return set_error(MOE_ERR_UNSUPPORTED, "num_tokens * ceil(K/512) must be below 2^31");
   if (a->sf_mode == MOE_SF_UE8M0_PACKED && a->x_sf_stride1 < 1 && (G + 3) / 4 > 1)
     return set_error(MOE_ERR_SHAPE, "x_sf stride1 must be positive");
+  if ((a->shared_x_sf != nullptr) != (a->shared_block_m != 0))
+    return set_error(MOE_ERR_INVALID_ARGUMENT,
+                     "shared_x_sf and shared_block_m must be given together");
+  if (a->shared_x_sf != nullptr) {
+    if (a->sf_mode != MOE_SF_UE8M0_PACKED)
+      return set_error(MOE_ERR_UNSUPPORTED, "shared_x_sf requires MOE_SF_UE8M0_PACKED scales");
+    if (a->shared_block_m < 0)
+      return set_error(MOE_ERR_INVALID_ARGUMENT, "shared_block_m must be positive");
+    const int64_t aligned = (a->shared_block_m + 127) / 128 * 128;
+    const int64_t need = (a->num_tokens + a->shared_block_m - 1) / a->shared_block_m * aligned;
+    if (a->shared_x_sf_rows < need)
+      return set_error(MOE_ERR_SHAPE, "shared_x_sf needs %lld rows, got %lld", (long long)need,
+                       (long long)a->shared_x_sf_rows);
+    if (a->shared_x_sf_stride0 < 1 || (G > 1 && a->shared_x_sf_stride1 < 1))
+      return set_error(MOE_ERR_SHAPE, "shared_x_sf strides must be positive");
+  }
   if (a->logical_to_physical != nullptr) {
     if (a->logical_replica_count == nullptr || a->num_logical <= 0 || a->map_stride <= 0)
       return set_error(MOE_ERR_INVALID_ARGUMENT,

@@ -41,6 +41,8 @@ struct StageParams {
   int64_t xs0;
   void* x_sf;
   int64_t sfs0, sfs1;
+  uint8_t* shared_sf;  // shared-expert scale pages (nullable)
+  int64_t ss0, ss1, sbm, sbm_aligned;
   int64_t* ids_out;
   int64_t ios0, ios1;
   float* w_out;
@@ -240,7 +242,7 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
 }
 
 // One task after its two loads have landed.
-template <int SF_MODE, bool DISPATCH>
+template <int SF_MODE, bool DISPATCH, bool SHARED>
 __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int64_t w, uint4 vA,
                                            uint4 vB, int lane) {
   const int half = lane >> 4;
@@ -272,6 +274,14 @@ __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int6
       const uint32_t e3w = __shfl_sync(0xFFFFFFFFu, b, 16);
       word = e0w | (e1w << 8) | (e2w << 16) | (e3w << 24);
       if (lane == 0) reinterpret_cast<uint32_t*>(p.x_sf)[t * p.sfs0 + w * p.sfs1] = word;
+      if (SHARED && lane < 4 && 4 * w + lane < p.G) {
+        // shared-expert pages: each 128-row page holds its four 32-token
+        // quarters interleaved row by row
+        const int64_t m = t % p.sbm;
+        const int64_t row = (t / p.sbm) * p.sbm_aligned + (m / 128) * 128 + (m % 32) * 4 +
+                            (m % 128) / 32;
+        p.shared_sf[row * p.ss0 + (4 * w + lane) * p.ss1] = (uint8_t)(word >> (8 * lane));
+      }
     } else {
       if ((lane & 15) == 0) {
         float* sf = reinterpret_cast<float*>(p.x_sf) + t * p.sfs0;
@@ -350,7 +360,7 @@ __device__ __forceinline__ void repack_recorded(const StageParams& p, int64_t r0
     if (s_load[i] != 0) atomicAdd(&p.load[i], s_load[i]);
 }
 
-template <int SF_MODE, bool REPACK, bool DISPATCH, typename IdT, typename WT>
+template <int SF_MODE, bool REPACK, bool DISPATCH, typename IdT, typename WT, bool SHARED>
 __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
   __shared__ int s_load[REPACK ? kLoadBins : 1];
   const int lane = threadIdx.x & 31;
@@ -393,7 +403,7 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
 #pragma unroll
     for (int i = 0; i < QUANT_BATCH; ++i) {
       if (base + i * nw < tasks)
-        quant_task<SF_MODE, DISPATCH>(p, cur.t[i], cur.w[i], cur.vA[i], cur.vB[i], lane);
+        quant_task<SF_MODE, DISPATCH, SHARED>(p, cur.t[i], cur.w[i], cur.vA[i], cur.vB[i], lane);
     }
     if (more) cur = nxt;
   }
@@ -464,24 +474,30 @@ static moe_status_t launch_typed(StageParams& p, bool dispatch, int sf_mode, cud
     cudaError_t le = launch_pdl(rk, dim3((unsigned)B), dim3(1024), smem, s, p);
     if (le != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "route_kernel launch: %s", cudaGetErrorString(le));
-    auto qk = moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT>;
+    // the shared-expert pages are a separate instantiation: even untaken,
+    // their code costs the streaming loop ~10%
+    auto qk = p.shared_sf != nullptr
+                  ? moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, true>
+                  : moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, false>;
     le = launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
     if (le != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "quant_kernel launch: %s", cudaGetErrorString(le));
   } else {
     switch (sf_mode) {
       case MOE_SF_NONE: {
-        auto qk = moe::quant_kernel<MOE_SF_NONE, true, false, IdT, WT>;
+        auto qk = moe::quant_kernel<MOE_SF_NONE, true, false, IdT, WT, false>;
         launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
         break;
       }
       case MOE_SF_UE8M0_PACKED: {
-        auto qk = moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT>;
+        auto qk = p.shared_sf != nullptr
+                      ? moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT, true>
+                      : moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT, false>;
         launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
         break;
       }
       default: {
-        auto qk = moe::quant_kernel<MOE_SF_FP32, true, false, IdT, WT>;
+        auto qk = moe::quant_kernel<MOE_SF_FP32, true, false, IdT, WT, false>;
         launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
         break;
       }
@@ -514,6 +530,11 @@ moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s) {
   p.x_sf = a->x_sf;
   p.sfs0 = a->x_sf_stride0;
   p.sfs1 = a->x_sf_stride1;
+  p.shared_sf = a->shared_x_sf;
+  p.ss0 = a->shared_x_sf_stride0;
+  p.ss1 = a->shared_x_sf_stride1;
+  p.sbm = a->shared_block_m > 0 ? a->shared_block_m : 1;
+  p.sbm_aligned = (p.sbm + 127) / 128 * 128;
   p.ids_out = a->topk_idx_out;
   p.ios0 = a->topk_idx_out_stride0;
   p.ios1 = a->topk_idx_out_stride1;

@@ -70,6 +70,10 @@ def _load():
         lib.orc_prepare_inputs.restype = i32
         lib.orc_prepare_inputs.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32, vp, vp,
                                            vp, vp, vp, i64, i64, vp, vp, i64, i32, i64]
+        lib.orc_shared_sf_row.restype = i64
+        lib.orc_shared_sf_row.argtypes = [i64, i64]
+        lib.orc_shared_sf.restype = None
+        lib.orc_shared_sf.argtypes = [i64, i64, vp, i64, vp, i64, i64]
         lib.orc_dispatch.restype = i32
         lib.orc_dispatch.argtypes = [i64, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, vp]
         lib.orc_w13_rows.restype = None
@@ -165,6 +169,28 @@ def prepare_inputs(hidden_bf16_bits, topk_ids, topk_weights, is_padding=None, sf
 
 
 # --------------------------------------------------------------------------- S6
+def shared_sf_row(t: int, block_m: int) -> int:
+    """Row of token t in the shared-expert scale pages (S4b)."""
+    return int(_load().orc_shared_sf_row(int(t), int(block_m)))
+
+
+def shared_sf(x_sf_words, K: int, block_m: int, rows: int | None = None, fill: int = 0xEE):
+    """Shared-expert scale pages of token-order packed exponents (S4b).
+
+    Returns uint8 [rows, K/128]; rows that no token maps to keep ``fill``.
+    """
+    lib = _load()
+    words = _c(x_sf_words, np.int32)
+    T = words.shape[0]
+    G = K // 128
+    padded = (block_m + 127) // 128 * 128
+    need = (T + block_m - 1) // block_m * padded
+    rows = need if rows is None else rows
+    out = np.full((rows, G), fill, np.uint8)
+    lib.orc_shared_sf(T, G, _p(words), int(block_m), _p(out), G, 1)
+    return out
+
+
 def dispatch(ids, x, x_sf_words, E, M_max, copy_rows=True):
     """Batched layout.  Returns dict(expert_num_tokens, route_slot, x_b, sf_b, status)."""
     lib = _load()

@@ -217,6 +217,38 @@ int orc_prepare_inputs(int64_t T, int64_t K, int64_t top_k, const uint16_t* hidd
 }
 
 /* ------------------------------------------------------------------------ */
+/* S4b: shared-expert scale pages (prepare_megamoe_inputs with shared_x_sf  */
+/* and shared_block_m; _shared_sf_row).  Token t sits in page block          */
+/* t / B (B = shared_block_m), whose rows are padded to a multiple of 128.   */
+/* Inside the block, position m = t % B is split into its 128-row page       */
+/* (m / 128) and, within that page, into quarter q = (m % 128) / 32 and      */
+/* offset i = m % 32; the page stores offset-major: row 4*i + q.  The        */
+/* exponent byte of group g lands in column g.                               */
+int64_t orc_shared_sf_row(int64_t t, int64_t block_m) {
+  const int64_t padded = ((block_m + 127) / 128) * 128;
+  const int64_t block = t / block_m;
+  const int64_t m = t % block_m;
+  const int64_t page = m / 128;
+  const int64_t quarter = (m % 128) / 32;
+  const int64_t offset = m % 32;
+  return block * padded + page * 128 + 4 * offset + quarter;
+}
+
+/* x_sf_words: [T, ceil(G/4)] packed exponents (S4) of the token-order      */
+/* staging; out: uint8 with strides (s0, s1); untouched outside the rows of  */
+/* the T tokens.                                                            */
+void orc_shared_sf(int64_t T, int64_t G, const int32_t* x_sf_words, int64_t block_m,
+                   uint8_t* out, int64_t s0, int64_t s1) {
+  const int64_t W = (G + 3) / 4;
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t row = orc_shared_sf_row(t, block_m);
+    for (int64_t g = 0; g < G; ++g) {
+      const uint32_t word = (uint32_t)x_sf_words[t * W + g / 4];
+      out[row * s0 + g * s1] = (uint8_t)((word >> (8 * (g % 4))) & 0xFFu);
+    }
+  }
+}
+
 /* S6: dispatch to the batched [E, M_max, .] layout.  Routes are visited in  */
 /* (token, k) order; each takes the next free slot of its expert.  A route   */
 /* whose expert is full is not placed (route_slot = -1) and the function     */

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
         assert must in names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/moe_prep.h but not exported"
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails its checks first
@@ -87,6 +87,19 @@ def test_prepare_rejects(lib):
     st, _ = _prep(lib, _prep_args(num_experts=2000, **{k: v for k, v in d.items()
                                                          if k != "num_experts"}))
     assert st == 2
+    # shared-expert scale pages: both or neither, UE8M0 only, enough rows
+    st, _ = _prep(lib, _prep_args(shared_x_sf=FAKE))
+    assert st == 1
+    st, _ = _prep(lib, _prep_args(shared_block_m=128))
+    assert st == 1
+    sh = dict(shared_x_sf=FAKE, shared_block_m=200, shared_x_sf_stride0=2,
+              shared_x_sf_stride1=1)
+    st, _ = _prep(lib, _prep_args(sf_mode=B.MOE_SF_FP32, shared_x_sf_rows=256, **sh))
+    assert st == 3
+    st, msg = _prep(lib, _prep_args(shared_x_sf_rows=255, **sh))
+    assert st == 2 and "256" in msg  # ceil(T/200) pages of 256 rows
+    st, _ = _prep(lib, _prep_args(shared_block_m=-4, shared_x_sf=FAKE))
+    assert st == 1
     # T == 0 is a no-op
     st, _ = _prep(lib, _prep_args(num_tokens=0))
     assert st == 0

@@ -217,3 +217,63 @@ def test_empty_batch_is_noop(cuda):
                          torch.zeros((0, 2), dtype=torch.int64, device=dev),
                          torch.zeros((0, 2), dtype=torch.float32, device=dev))
     torch.cuda.synchronize()
+
+
+def _shared_pages(hidden, ids, w, block_m, dispatch=None, fill=0xEE, extra_rows=5):
+    dev = torch.device("cuda")
+    T, K = hidden.shape
+    G = K // 128
+    padded = (block_m + 127) // 128 * 128
+    rows = (T + block_m - 1) // block_m * padded + extra_rows
+    shared = torch.full((rows, G), fill, dtype=torch.uint8, device=dev)
+    x = torch.empty((T, K), dtype=torch.uint8, device=dev)
+    x_sf = torch.empty((T, (G + 3) // 4), dtype=torch.int32, device=dev)
+    k = ids.shape[1]
+    ids_out = torch.empty((T, k), dtype=torch.int64, device=dev)
+    w_out = torch.empty((T, k), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.moe_prepare_inputs(hidden.to(dev), ids.to(dev), w.to(dev), x, x_sf, ids_out, w_out,
+                         dispatch=dispatch, device_status=status, shared_x_sf=shared,
+                         shared_block_m=block_m)
+    torch.cuda.synchronize()
+    return shared.cpu().numpy(), x_sf.cpu().numpy(), int(status.item())
+
+
+@pytest.mark.parametrize("T,K,block_m", [
+    (300, 896, 200),    # G = 7: ragged last word; partial pages
+    (300, 896, 1),      # one token per block
+    (257, 256, 128),    # whole pages plus one token
+    (1000, 7168, 256),  # DeepSeek-V3 hidden size
+    (64, 4096, 64),     # block smaller than a page
+])
+def test_shared_scale_pages(cuda, orc, T, K, block_m):
+    """Shared-expert scale pages: every token's exponent bytes at its page
+    row, bit-exact with the oracle; rows no token maps to stay untouched."""
+    hid = syn.make_hidden(T, K, 7 + T, outlier_frac=0.01, zero_group_frac=0.05)
+    ids, w, _ = syn.make_routing(T, 8, 2, 8 + T)
+    shared, x_sf, st = _shared_pages(hid, ids, w, block_m)
+    assert st == 0
+    ref = orc.prepare_inputs(bf16_bits(hid), ids.numpy(), w.numpy())
+    assert np.array_equal(x_sf, ref["x_sf"])
+    want = orc.shared_sf(ref["x_sf"], K, block_m, rows=shared.shape[0], fill=0xEE)
+    assert np.array_equal(shared, want)
+
+
+def test_shared_scale_pages_with_dispatch(cuda, orc):
+    """The pages are written in token order also when the rows are dispatched."""
+    T, K, k, E, M_max = 128, 7168, 8, 256, 128
+    hid, ids, w, pad = _dispatch_case(T, K, k, E, M_max, 1.1, 0.0, seed=3)
+    dev = torch.device("cuda")
+    Wd = (K // 128 + 3) // 4
+    disp = dict(num_experts=E, max_tokens_per_expert=M_max,
+                x_b=torch.empty((E * M_max, K), dtype=torch.uint8, device=dev),
+                sf_b=torch.empty((E * M_max, Wd), dtype=torch.int32, device=dev),
+                expert_num_tokens=torch.empty((E,), dtype=torch.int32, device=dev),
+                route_slot=torch.empty((T, k), dtype=torch.int32, device=dev),
+                workspace=torch.empty(B.prepare_workspace_size(T, k, E), dtype=torch.uint8,
+                                      device=dev))
+    shared, x_sf, st = _shared_pages(hid, ids, w, 96, dispatch=disp)
+    assert st == 0
+    ref = orc.prepare_inputs(bf16_bits(hid), ids.numpy(), w.numpy())
+    want = orc.shared_sf(ref["x_sf"], K, 96, rows=shared.shape[0], fill=0xEE)
+    assert np.array_equal(shared, want)
