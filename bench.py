@@ -70,6 +70,8 @@ def parse():
     ap.add_argument("--config", default="mixtral_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--layout", default="batched", choices=["batched", "contiguous"],
+                    help="expert row layout: [E, M_max] slots or expert_offsets")
     return ap.parse_args()
 
 
@@ -253,7 +255,8 @@ def bench_ours(args, world, rank, local):
         return bench_staging(args, world, rank, dev, wl, peaks, flush)
 
     layer = B.MoeLayer(c["T"], c["K"], c["N"], c["E"], c["top_k"], c["M_max"], wl["w13"],
-                       wl["w13_s"], wl["w2"], wl["w2_s"], device=dev)
+                       wl["w13_s"], wl["w2"], wl["w2_s"], device=dev,
+                       contiguous=args.layout == "contiguous")
     hid, ids, wts, pad = (wl["hidden"].to(dev), wl["topk_ids"].to(dev),
                           wl["topk_weights"].to(dev), wl["is_padding"].to(dev))
     inter_q, inter_sf = layer.inter()
@@ -267,14 +270,15 @@ def bench_ours(args, world, rank, local):
         B.moe_batched_experts(layer.out_b, layer.x_b, layer.sf_b, layer.w13, layer.w13_s,
                               layer.w2, layer.w2_s, layer.expert_num_tokens, layer.ws13,
                               layer.ws2, valid_shape_m=layer.valid_shape_m,
-                              stages=B.MOE_STAGE_W13, device_status=layer.status)
+                              stages=B.MOE_STAGE_W13, device_status=layer.status,
+                              expert_offsets=layer.expert_offsets)
         if evs:
             evs[2].record(s)
         B.moe_batched_experts(layer.out_b, None, None, layer.w13, layer.w13_s, layer.w2,
                               layer.w2_s, layer.expert_num_tokens, layer.ws13, layer.ws2,
                               valid_shape_m=layer.valid_shape_m, inter_q=inter_q,
                               inter_sf=inter_sf, stages=B.MOE_STAGE_W2,
-                              device_status=layer.status)
+                              device_status=layer.status, expert_offsets=layer.expert_offsets)
         if evs:
             evs[3].record(s)
         layer.reduce()
@@ -363,7 +367,8 @@ def bench_ours(args, world, rank, local):
                scaling="weak", vs_baseline=None, dtype="fp8e4m3 (fp32 accumulate)",
                data="synthetic",
                config=dict(workload=name, T=c["T"], K=c["K"], N=c["N"], E=c["E"],
-                           top_k=c["top_k"], M_max=c["M_max"], routed_rows=alg["R"],
+                           top_k=c["top_k"], M_max=layer.M_max, layout=args.layout,
+                           routed_rows=alg["R"],
                            active_experts=alg["A"],
                            l2="inputs larger than L2 and a 512 MB L2 flush before every step",
                            parallelism=f"replicas x{world}"),

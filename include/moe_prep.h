@@ -95,6 +95,14 @@ typedef enum moe_activation { MOE_ACT_SILU = 0 } moe_activation_t;
 /* sf_b[e, s, :] = x_sf[t, :], route_slot[t, j] = s (-1 when unrouted or     */
 /* when s >= max_tokens_per_expert, which also sets MOE_DEV_CAPACITY),       */
 /* expert_num_tokens[e] = min(#routes to e, max_tokens_per_expert).          */
+/* Contiguous layout (when expert_offsets != NULL; the expert_offsets /     */
+/* moe_permute layout of HummingGroupedExperts.apply on the experts page):  */
+/* no per-expert capacity; the routes of expert e fill rows                 */
+/* [expert_offsets[e], expert_offsets[e+1]) of x_b / sf_b in the same       */
+/* (token, k) order, expert_offsets[e] = #routes to experts < e,            */
+/* expert_offsets[E] = #routes, route_slot[t, j] = the row (not the slot)   */
+/* and expert_num_tokens[e] the full count.  x_b / sf_b hold                */
+/* E * max_tokens_per_expert rows, which must be >= T * k (else SHAPE).     */
 /*                                                                           */
 /* Shared-expert scale pages (when shared_x_sf != NULL; defined by the      */
 /* shared_x_sf / shared_block_m arguments of prepare_megamoe_inputs and by   */
@@ -161,6 +169,7 @@ typedef struct moe_prepare_args {
   int32_t* sf_b;                 /* int32 [E, M_max, ceil(G/4)] */
   int32_t* expert_num_tokens;    /* int32 [E] */
   int32_t* route_slot;           /* int32 [T, k], contiguous */
+  int32_t* expert_offsets;       /* nullable int32 [E + 1]: contiguous layout */
   void* workspace;               /* moe_prepare_workspace_size() bytes */
   size_t workspace_bytes;
 
@@ -228,6 +237,12 @@ moe_status_t moe_prepare_inputs_noalloc(const moe_prepare_args_t* args, void* st
 /* inter_q fp8 [E*M_max, N] and inter_sf int32 [E*M_max, ceil(Gn/4)] may be  */
 /* NULL, in which case they are carved from workspace13.  With stages ==     */
 /* MOE_STAGE_W2 the caller supplies them (the w2 stage alone).               */
+/* Contiguous layout (expert_offsets != NULL, [E+1] as written by           */
+/* moe_prepare_inputs; HummingGroupedExperts.apply with expert_layout =     */
+/* expert_offsets): expert e owns rows [expert_offsets[e],                  */
+/* expert_offsets[e+1]) of x_b / a_scale / inter_q / inter_sf / output,     */
+/* which are still E*M_max rows long (expert_offsets[E] <= E*M_max), and     */
+/* its row count is not capped by M_max.                                     */
 /* workspace2 holds split-K partials and tile counters.  It must be zero-    */
 /* filled once when allocated; every call leaves its counters at zero again   */
 /* (after a MOE_DEV_TIMEOUT, zero it before reuse).                           */
@@ -251,6 +266,7 @@ typedef struct moe_experts_args {
   const void* w2;                     /* fp8 [E, K, N] */
   const float* w2_scale;              /* [E, K/128, N/128] */
   const int32_t* expert_num_tokens;   /* [E] */
+  const int32_t* expert_offsets;      /* nullable [E+1]: contiguous layout */
 
   void* inter_q;   /* nullable: fp8 [E*M_max, N] */
   void* inter_sf;  /* nullable: int32 [E*M_max, ceil(Gn/4)] */
@@ -284,6 +300,9 @@ size_t moe_batched_experts_workspace_size(int64_t num_experts, int64_t max_token
 /* expert_out bf16 [E, M_max, K]; topk_idx int64 [T, k]; route_slot int32    */
 /* [T, k]; topk_weights fp32 [T, k]; out bf16 [T, K]; all contiguous; the    */
 /* expert_out and out base pointers 16-byte aligned; K % 8 == 0.             */
+/* Contiguous layout (moe_unpermute of HummingGroupedExperts.apply): with    */
+/* topk_idx == NULL, route_slot[t, j] is the row of expert_out itself (-1 =  */
+/* unplaced), rows < num_experts * max_tokens_per_expert.                    */
 /* ------------------------------------------------------------------------ */
 moe_status_t moe_topk_reduce(const void* expert_out, int64_t num_experts,
                              int64_t max_tokens_per_expert, int64_t hidden_size,

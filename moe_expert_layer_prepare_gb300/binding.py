@@ -50,6 +50,7 @@ class PrepareArgs(ctypes.Structure):
         ("should_record", _vp), ("num_unpadded_tokens", _vp),
         ("num_experts", _i64), ("max_tokens_per_expert", _i64),
         ("x_b", _vp), ("sf_b", _vp), ("expert_num_tokens", _vp), ("route_slot", _vp),
+        ("expert_offsets", _vp),
         ("workspace", _vp), ("workspace_bytes", _sz),
         ("device_status", _vp),
     ]
@@ -61,7 +62,7 @@ class ExpertsArgs(ctypes.Structure):
         ("intermediate_size", _i64), ("activation", _i32), ("stages", _i32),
         ("output", _vp), ("hidden", _vp), ("a_scale", _vp), ("a_scale_mode", _i32),
         ("w13", _vp), ("w13_scale", _vp), ("w2", _vp), ("w2_scale", _vp),
-        ("expert_num_tokens", _vp),
+        ("expert_num_tokens", _vp), ("expert_offsets", _vp),
         ("inter_q", _vp), ("inter_sf", _vp),
         ("workspace13", _vp), ("workspace13_bytes", _sz),
         ("workspace2", _vp), ("workspace2_bytes", _sz),
@@ -140,7 +141,8 @@ def moe_prepare_inputs(hidden, topk_ids, topk_weights, x, x_sf, topk_idx_out, to
     eplb: dict(logical_to_physical, logical_replica_count, expert_load=None,
                should_record=None, num_unpadded_tokens=None) -- device tensors.
     dispatch: dict(num_experts, max_tokens_per_expert, x_b, sf_b, expert_num_tokens,
-                   route_slot, workspace).
+                   route_slot, workspace[, expert_offsets]) -- with expert_offsets
+              ([E+1] int32) the rows are laid out contiguously per expert.
     """
     T, K = hidden.shape
     a = PrepareArgs()
@@ -187,6 +189,7 @@ def moe_prepare_inputs(hidden, topk_ids, topk_weights, x, x_sf, topk_idx_out, to
         a.x_b, a.sf_b = _ptr(dispatch["x_b"]), _ptr(dispatch["sf_b"])
         a.expert_num_tokens = _ptr(dispatch["expert_num_tokens"])
         a.route_slot = _ptr(dispatch["route_slot"])
+        a.expert_offsets = _ptr(dispatch.get("expert_offsets"))
         ws = dispatch["workspace"]
         a.workspace, a.workspace_bytes = _ptr(ws), ws.numel() * ws.element_size()
     a.device_status = _ptr(device_status)
@@ -252,12 +255,18 @@ def moe_prepare_inputs_noalloc(hidden, topk_ids, topk_weights, x, x_sf, topk_idx
 def moe_batched_experts(output, hidden, a_scale, w13, w13_scale, w2, w2_scale,
                         expert_num_tokens, workspace13=None, workspace2=None, valid_shape_m=0,
                         inter_q=None, inter_sf=None, gate_up_dump=None, stages=MOE_STAGE_ALL,
-                        device_status=None, stream=None):
-    """w13 GEMM + SiLU-and-mul requant + w2 GEMM.  See include/moe_prep.h."""
+                        device_status=None, stream=None, expert_offsets=None):
+    """w13 GEMM + SiLU-and-mul requant + w2 GEMM.  See include/moe_prep.h.
+
+    expert_offsets ([E+1] int32, nullable) selects the contiguous layout.
+    """
     E = w13.shape[0]
     K = w13.shape[2]
     N = w2.shape[2]
-    M_max = (output.shape[1] if output is not None else hidden.shape[0] // E)
+    if output is not None:
+        M_max = output.shape[1] if output.dim() == 3 else output.shape[0] // E
+    else:
+        M_max = hidden.shape[0] // E
     a = ExpertsArgs()
     a.num_experts, a.max_tokens_per_expert, a.hidden_size, a.intermediate_size = E, M_max, K, N
     a.activation, a.stages = MOE_ACT_SILU, stages
@@ -265,6 +274,7 @@ def moe_batched_experts(output, hidden, a_scale, w13, w13_scale, w2, w2_scale,
     a.a_scale_mode = MOE_SF_UE8M0_PACKED
     a.w13, a.w13_scale, a.w2, a.w2_scale = _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale)
     a.expert_num_tokens = _ptr(expert_num_tokens)
+    a.expert_offsets = _ptr(expert_offsets)
     a.inter_q, a.inter_sf = _ptr(inter_q), _ptr(inter_sf)
     if workspace13 is not None:
         a.workspace13 = _ptr(workspace13)
@@ -279,9 +289,15 @@ def moe_batched_experts(output, hidden, a_scale, w13, w13_scale, w2, w2_scale,
 
 
 def moe_topk_reduce(expert_out, topk_idx, route_slot, topk_weights, out, stream=None):
-    """Top-k weighted sum back to token order.  See include/moe_prep.h."""
-    E, M_max, K = expert_out.shape
-    T, k = topk_idx.shape
+    """Top-k weighted sum back to token order.  See include/moe_prep.h.
+
+    topk_idx None: route_slot holds rows of expert_out (contiguous layout).
+    """
+    if expert_out.dim() == 3:
+        E, M_max, K = expert_out.shape
+    else:
+        (E, K), M_max = (1, expert_out.shape[1]), expert_out.shape[0]
+    T, k = route_slot.shape
     _check("moe_topk_reduce", load().moe_topk_reduce(
         _ptr(expert_out), E, M_max, K, _ptr(topk_idx), _ptr(route_slot), _ptr(topk_weights), T, k,
         _ptr(out), _stream(stream)))
@@ -295,7 +311,12 @@ class MoeLayer:
     """
 
     def __init__(self, T, K, N, E, top_k, M_max, w13, w13_s, w2, w2_s, device="cuda",
-                 valid_shape_m=None, eplb=None):
+                 valid_shape_m=None, eplb=None, contiguous=False):
+        # contiguous: rows are packed per expert (expert_offsets); the buffers
+        # hold E * ceil(T*k/E) rows, whatever the per-expert load
+        if contiguous:
+            M_max = max(1, -(-(T * top_k) // E))
+        self.contiguous = contiguous
         self.T, self.K, self.N, self.E, self.top_k, self.M_max = T, K, N, E, top_k, M_max
         self.w13, self.w13_s, self.w2, self.w2_s = w13, w13_s, w2, w2_s
         self.eplb = eplb
@@ -311,6 +332,8 @@ class MoeLayer:
         self.sf_b = torch.empty((E * M_max, W), dtype=torch.int32, device=dev)
         self.expert_num_tokens = torch.zeros(E, dtype=torch.int32, device=dev)
         self.route_slot = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+        self.expert_offsets = (torch.zeros(E + 1, dtype=torch.int32, device=dev) if contiguous
+                               else None)
         self.ws_prep = torch.empty(max(prepare_workspace_size(T, top_k, E), 256), **u8)
         self.valid_shape_m = valid_shape_m if valid_shape_m is not None else T * top_k
         self.ws13 = torch.empty(experts_workspace_size(E, M_max, K, N, self.valid_shape_m, 13), **u8)
@@ -323,7 +346,8 @@ class MoeLayer:
     def dispatch_args(self):
         return dict(num_experts=self.E, max_tokens_per_expert=self.M_max, x_b=self.x_b,
                     sf_b=self.sf_b, expert_num_tokens=self.expert_num_tokens,
-                    route_slot=self.route_slot, workspace=self.ws_prep)
+                    route_slot=self.route_slot, workspace=self.ws_prep,
+                    expert_offsets=self.expert_offsets)
 
     def prepare(self, hidden, topk_ids, topk_weights, is_padding=None, stream=None):
         moe_prepare_inputs(hidden, topk_ids, topk_weights, self.x, self.x_sf, self.ids_out,
@@ -335,11 +359,12 @@ class MoeLayer:
         moe_batched_experts(self.out_b, self.x_b, self.sf_b, self.w13, self.w13_s, self.w2,
                             self.w2_s, self.expert_num_tokens, self.ws13, self.ws2,
                             valid_shape_m=self.valid_shape_m, gate_up_dump=gate_up_dump,
-                            device_status=self.status, stream=stream)
+                            device_status=self.status, stream=stream,
+                            expert_offsets=self.expert_offsets)
 
     def reduce(self, stream=None):
-        moe_topk_reduce(self.out_b, self.ids_out, self.route_slot, self.w_out, self.out,
-                        stream=stream)
+        moe_topk_reduce(self.out_b, None if self.contiguous else self.ids_out, self.route_slot,
+                        self.w_out, self.out, stream=stream)
 
     def forward(self, hidden, topk_ids, topk_weights, is_padding=None, stream=None):
         self.prepare(hidden, topk_ids, topk_weights, is_padding, stream)

@@ -147,6 +147,13 @@ moe_status_t moe_prepare_inputs(const moe_prepare_args_t* a, void* stream) {
                        a->workspace_bytes);
     if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
       return set_error(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+    if (a->expert_offsets != nullptr &&
+        a->num_tokens * a->top_k > a->num_experts * a->max_tokens_per_expert)
+      return set_error(MOE_ERR_SHAPE,
+                       "contiguous layout needs num_experts * max_tokens_per_expert >= %lld rows",
+                       (long long)(a->num_tokens * a->top_k));
+  } else if (a->expert_offsets != nullptr) {
+    return set_error(MOE_ERR_INVALID_ARGUMENT, "expert_offsets needs the dispatch outputs (x_b)");
   }
   return launch_prepare(a, static_cast<cudaStream_t>(stream));
 }
@@ -229,7 +236,8 @@ moe_status_t moe_topk_reduce(const void* expert_out, int64_t num_experts,
   if (hidden_size % 8 != 0) return set_error(MOE_ERR_SHAPE, "hidden_size must be a multiple of 8");
   if (num_tokens * ((hidden_size + 255) / 256) >= ((int64_t)1 << 31))
     return set_error(MOE_ERR_UNSUPPORTED, "num_tokens * ceil(K/256) must be below 2^31");
-  if (!expert_out || !out || (top_k > 0 && (!topk_idx || !route_slot || !topk_weights)))
+  // topk_idx == NULL: route_slot holds rows of expert_out (contiguous layout)
+  if (!expert_out || !out || (top_k > 0 && (!route_slot || !topk_weights)))
     return set_error(MOE_ERR_INVALID_ARGUMENT, "a required pointer is NULL");
   if (!aligned16(expert_out) || !aligned16(out))
     return set_error(MOE_ERR_ALIGNMENT, "expert_out and out must be 16-byte aligned");

@@ -74,6 +74,7 @@ struct GemmParams {
   int K;           // hidden size
   int b_rows;      // rows of one expert in the B tensor (2N or K)
   const int32_t* expert_num_tokens;
+  const int32_t* offsets;  // contiguous layout: [E+1] first row of each expert (nullable)
   const uint32_t* a_sf;  // packed UE8M0 words [E*M_max, Wa]
   int Wa;
   const float* w_s;      // [E, b_rows/128, KB]
@@ -85,7 +86,7 @@ struct GemmParams {
   // w2 outputs
   uint16_t* out;         // bf16 [E*M_max, K]
   float* partials;       // [splits, E*M_max, K]
-  int32_t* counters;     // [E * mt_max * n_tiles]
+  int32_t* counters;     // [(E * mt_max + E) * n_tiles]
   int mt_max;
   int32_t* zero_counters;  // w13 zeroes the next w2's counters
   int n_zero_counters;
@@ -272,6 +273,8 @@ __device__ __forceinline__ void tmem_wait_ld() {
 // ------------------------------------------------------------------ schedule
 struct Unit {
   int e, mt, nt, ks, rows, kb0, kb1;
+  int row0;  // first row of the tile in the [E*M_max, .] buffers
+  int gmt;   // global m-tile index (split-K counters of the contiguous layout)
 };
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const int* prefix, int u,
@@ -290,6 +293,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const int* pref
   w.e = lo;
   w.mt = mt_idx - prefix[lo];
   w.rows = min(BM, cnt[lo] - w.mt * BM);
+  w.row0 = (p.offsets != nullptr ? __ldg(p.offsets + lo) : lo * p.M_max) + w.mt * BM;
+  w.gmt = mt_idx;
   const int per = (p.KB + p.splits - 1) / p.splits;
   w.kb0 = w.ks * per;
   w.kb1 = min(p.KB, w.kb0 + per);
@@ -363,8 +368,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   // Per-expert row counts and the exclusive prefix of m-tiles.
   for (int e = tid; e < p.E; e += NUM_THREADS) {
-    int n = p.expert_num_tokens[e];
-    n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
+    int n;
+    if (p.offsets == nullptr) {
+      n = p.expert_num_tokens[e];
+      n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
+    } else {
+      // contiguous layout: rows [offsets[e], offsets[e+1]), kept inside the
+      // E*M_max-row buffers whatever the offsets say
+      const int64_t rows_total = (int64_t)p.E * p.M_max;
+      const int64_t o0 = p.offsets[e], o1 = p.offsets[e + 1];
+      n = (o0 < 0 || o1 <= o0 || o0 >= rows_total) ? 0 : (int)min(o1, rows_total) - (int)o0;
+    }
     cnt[e] = n;
   }
   __syncthreads();
@@ -402,7 +416,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         const Unit w = decode_unit(p, prefix, u, cnt);
-        const int a_row0 = w.e * p.M_max + w.mt * BM;
+        const int a_row0 = w.row0;
         const int n_boxes = (w.rows + A_BOX_ROWS - 1) / A_BOX_ROWS;
         const uint32_t tx = (uint32_t)(n_boxes * A_BOX_ROWS * BK + B_BYTES);
         int b_row0, b_row1;
@@ -526,7 +540,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Unit w = decode_unit(p, prefix, u, cnt);
       const bool row_ok = row_local < w.rows;
       const bool warp_active = q * 32 < w.rows;   // warp-uniform
-      const int64_t grow = (int64_t)w.e * p.M_max + (int64_t)w.mt * BM + row_local;
+      const int64_t grow = (int64_t)w.row0 + row_local;
       int nb0, nb1;
       if constexpr (W13) {
         nb0 = w.nt;                         // gate block
@@ -704,7 +718,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           __threadfence();
           epi_sync();
-          int32_t* ctr = p.counters + ((int64_t)w.e * p.mt_max + w.mt) * p.n_tiles + w.nt;
+          const int64_t ctr_row =
+              p.offsets != nullptr ? (int64_t)w.gmt : (int64_t)w.e * p.mt_max + w.mt;
+          int32_t* ctr = p.counters + ctr_row * p.n_tiles + w.nt;
           if (tid == EPI_WARP0 * 32) {
             const int prev = atomicAdd(ctr, 1);
             *s_flag = (prev == p.splits - 1) ? 1 : 0;
@@ -836,7 +852,7 @@ size_t experts_workspace_size(int64_t E, int64_t M_max, int64_t K, int64_t N, in
   const int S = w2_splits(E, M_max, K, N, vsm);
   const int64_t nt = (K + 255) / 256;
   const int64_t mt_max = (M_max + 127) / 128;
-  size_t bytes = (size_t)(((E * mt_max * nt * 4) + 255) / 256) * 256;
+  size_t bytes = (size_t)((((E * mt_max + E) * nt * 4) + 255) / 256) * 256;
   if (S > 1) bytes += (size_t)S * EM * K * 4;
   return bytes;
 }
@@ -872,7 +888,7 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
   if (stages & MOE_STAGE_W2) {
     char* ws2 = static_cast<char*>(a->workspace2);
     counters = reinterpret_cast<int32_t*>(ws2);
-    partials = reinterpret_cast<float*>(ws2 + ((E * mt_max * nt2 * 4 + 255) / 256) * 256);
+    partials = reinterpret_cast<float*>(ws2 + (((E * mt_max + E) * nt2 * 4 + 255) / 256) * 256);
   }
   const size_t smem = gemm_smem_bytes();
   const int sms = num_sms();
@@ -897,7 +913,8 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
     attr_done[0] = true;
   }
   // Upper bound of the work units: every expert full.  Persistent grid.
-  const int64_t mt_cap = E * mt_max;
+  // (the contiguous layout has at most E + E*M/128 m-tiles)
+  const int64_t mt_cap = E * mt_max + E;
 
   if (stages & MOE_STAGE_W13) {
     GemmParams p{};
@@ -911,6 +928,7 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
     p.K = (int)K;
     p.b_rows = (int)(2 * N);
     p.expert_num_tokens = a->expert_num_tokens;
+    p.offsets = a->expert_offsets;
     p.a_sf = static_cast<const uint32_t*>(a->a_scale);
     p.Wa = (int)((K / 128 + 3) / 4);
     p.w_s = a->w13_scale;
@@ -922,7 +940,7 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
     p.status = a->device_status;
     if ((stages & MOE_STAGE_W2) && S > 1) {
       p.zero_counters = counters;
-      p.n_zero_counters = (int)(E * mt_max * nt2);
+      p.n_zero_counters = (int)((E * mt_max + E) * nt2);
     }
     CUtensorMap tA, tB;
     if (!make_map(&tA, a->hidden, (uint64_t)EM, (uint64_t)K, moe::A_BOX_ROWS) ||
@@ -946,6 +964,7 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
     p.K = (int)K;
     p.b_rows = (int)K;
     p.expert_num_tokens = a->expert_num_tokens;
+    p.offsets = a->expert_offsets;
     p.a_sf = inter_sf;
     p.Wa = (int)Wy;
     p.w_s = a->w2_scale;

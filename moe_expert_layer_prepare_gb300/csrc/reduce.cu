@@ -17,7 +17,7 @@ namespace moe {
 struct ReduceParams {
   const uint16_t* expert_out;  // bf16 [E*M_max, K]
   int64_t E, M_max, K;
-  const int64_t* idx;    // [T, k]
+  const int64_t* idx;    // [T, k]; NULL: slot is the row (contiguous layout)
   const int32_t* slot;   // [T, k]
   const float* w;        // [T, k]
   int64_t T, top_k;
@@ -42,12 +42,19 @@ __global__ void __launch_bounds__(256) topk_reduce_kernel(ReduceParams p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
     for (int64_t j = 0; j < p.top_k; ++j) {
-      const int64_t e = p.idx[t * p.top_k + j];
       const int32_t s = p.slot[t * p.top_k + j];
-      if (e < 0 || s < 0 || e >= p.E || s >= p.M_max) continue;
+      int64_t row;
+      if (p.idx != nullptr) {  // batched: (expert, slot)
+        const int64_t e = p.idx[t * p.top_k + j];
+        if (e < 0 || s < 0 || e >= p.E || s >= p.M_max) continue;
+        row = e * p.M_max + s;
+      } else {  // contiguous: the slot is the row
+        if (s < 0 || s >= p.E * p.M_max) continue;
+        row = s;
+      }
       const float wt = p.w[t * p.top_k + j];
       if (active) {
-        const uint4 v = ld_stream_v4(p.expert_out + (e * p.M_max + s) * p.K + c0);
+        const uint4 v = ld_stream_v4(p.expert_out + row * p.K + c0);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {

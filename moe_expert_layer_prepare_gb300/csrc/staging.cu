@@ -60,6 +60,7 @@ struct StageParams {
   int32_t* sf_b;
   int32_t* expert_num_tokens;
   int32_t* route_slot;
+  int32_t* offsets;     // contiguous layout: [E+1] first row of each expert (nullable)
   int32_t* hist;        // [B, E] -> exclusive offsets after the scan
   int32_t* local_rank;  // [T*k]
   uint32_t* done;       // block completion counter (zeroed by the host)
@@ -178,17 +179,52 @@ __global__ void __launch_bounds__(1024) route_kernel(StageParams p) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // Last block: column-wise exclusive scan of hist over blocks.
+  // Last block: column-wise exclusive scan of hist over blocks (E <= 1024,
+  // so each thread owns at most one expert).
   const int64_t B = p.num_route_blocks;
-  for (int ex = tid; ex < E; ex += 1024) {
-    int run = 0;
+  int run = 0;
+  if (tid < E) {
     for (int64_t b = 0; b < B; ++b) {
-      int v = __ldcg(&p.hist[b * E + ex]);
-      p.hist[b * E + ex] = run;
+      int v = __ldcg(&p.hist[b * E + tid]);
+      p.hist[b * E + tid] = run;
       run += v;
     }
-    if (run > p.M_max) set_status(p.status, MOE_DEV_CAPACITY);
-    p.expert_num_tokens[ex] = (int32_t)min((int64_t)run, p.M_max);
+  }
+  if (p.offsets == nullptr) {
+    if (tid < E) {
+      if (run > p.M_max) set_status(p.status, MOE_DEV_CAPACITY);
+      p.expert_num_tokens[tid] = (int32_t)min((int64_t)run, p.M_max);
+    }
+  } else {
+    // Contiguous layout: exclusive scan of the per-expert totals over the
+    // experts gives each expert's first row; it is added to every block's
+    // offset so that a route's slot becomes its row.
+    __shared__ int s_warp_tot[32];
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int v = s_warp_tot[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (lane >= off) v += o;
+      }
+      s_warp_tot[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    const int base = incl - run + (warp > 0 ? s_warp_tot[warp - 1] : 0);
+    if (tid < E) {
+      for (int64_t b = 0; b < B; ++b) p.hist[b * E + tid] += base;
+      p.offsets[tid] = base;
+      p.expert_num_tokens[tid] = run;
+    }
+    if (tid == E - 1) p.offsets[E] = base + run;
   }
   if (tid == 0) *p.done = 0u;
 }
@@ -295,16 +331,24 @@ __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int6
       for (int64_t j = 0; j < p.top_k; ++j) {
         const int64_t r = t * p.top_k + j;
         const int64_t e = p.ids_out[t * p.ios0 + j * p.ios1];
-        int64_t slot = -1;
+        int64_t slot = -1, row = -1;
         if (e >= 0 && e < p.E) {
+          // contiguous layout: the scanned offsets already include the
+          // expert's first row, so the slot is the row
           slot = (int64_t)__ldcg(&p.hist[(r >> 10) * p.E + e]) + p.local_rank[r];
-          if (slot >= p.M_max) slot = -1;
+          if (p.offsets != nullptr) {
+            row = slot;
+          } else if (slot < p.M_max) {
+            row = e * p.M_max + slot;
+          } else {
+            slot = -1;
+          }
         }
         if (slot >= 0) {
-          uint8_t* brow = p.x_b + (e * p.M_max + slot) * K;
+          uint8_t* brow = p.x_b + row * K;
           if (actA) st_v2(brow + offA, qA);
           if (actB) st_v2(brow + offB, qB);
-          if (lane == 0) p.sf_b[(e * p.M_max + slot) * p.W + w] = (int32_t)word;
+          if (lane == 0) p.sf_b[row * p.W + w] = (int32_t)word;
         }
         if (w == 0 && lane == 0) p.route_slot[r] = (int32_t)slot;
       }
@@ -558,6 +602,7 @@ moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s) {
     p.sf_b = a->sf_b;
     p.expert_num_tokens = a->expert_num_tokens;
     p.route_slot = a->route_slot;
+    p.offsets = a->expert_offsets;
     const int64_t R = p.T * p.top_k;
     const int64_t B = (R + 1023) / 1024;
     char* ws = static_cast<char*>(a->workspace);

@@ -74,14 +74,16 @@ def _load():
         lib.orc_shared_sf_row.argtypes = [i64, i64]
         lib.orc_shared_sf.restype = None
         lib.orc_shared_sf.argtypes = [i64, i64, vp, i64, vp, i64, i64]
+        lib.orc_dispatch_contiguous.restype = i32
+        lib.orc_dispatch_contiguous.argtypes = [i64, i64, i64, vp, vp, vp, i64, vp, vp, vp, vp, vp]
         lib.orc_dispatch.restype = i32
         lib.orc_dispatch.argtypes = [i64, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, vp]
         lib.orc_w13_rows.restype = None
-        lib.orc_w13_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_w13_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.orc_silu_requant_rows.restype = None
         lib.orc_silu_requant_rows.argtypes = [i64, vp, i64, vp, vp, vp]
         lib.orc_w2_rows.restype = None
-        lib.orc_w2_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp]
+        lib.orc_w2_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp]
         lib.orc_topk_reduce.restype = None
         lib.orc_topk_reduce.argtypes = [i64, i64, i64, i64, vp, vp, vp, vp, vp]
         _lib = lib
@@ -209,6 +211,28 @@ def dispatch(ids, x, x_sf_words, E, M_max, copy_rows=True):
     return dict(expert_num_tokens=ent, route_slot=slot, x_b=x_b, sf_b=sf_b, status=int(st))
 
 
+def dispatch_contiguous(ids, x, x_sf_words, E):
+    """Contiguous layout (S6b).  Returns dict(expert_offsets, expert_num_tokens,
+    route_row, x_c, sf_c, row_expert, status); x_c / sf_c have T*k rows."""
+    lib = _load()
+    ids = _c(ids, np.int64)
+    T, top_k = ids.shape
+    x = _c(x, np.uint8)
+    K = x.shape[1]
+    sfw = _c(x_sf_words, np.int32)
+    W = sfw.shape[1]
+    offs = np.zeros(E + 1, np.int32)
+    ent = np.zeros(E, np.int32)
+    row = np.zeros((T, top_k), np.int32)
+    x_c = np.zeros((max(T * top_k, 1), K), np.uint8)
+    sf_c = np.zeros((max(T * top_k, 1), W), np.int32)
+    st = lib.orc_dispatch_contiguous(T, top_k, K, _p(ids), _p(x), _p(sfw), E, _p(offs), _p(ent),
+                                     _p(row), _p(x_c), _p(sf_c))
+    row_expert = np.repeat(np.arange(E, dtype=np.int64), ent)
+    return dict(expert_offsets=offs, expert_num_tokens=ent, route_row=row, x_c=x_c, sf_c=sf_c,
+                row_expert=row_expert, status=int(st))
+
+
 # --------------------------------------------------------------------------- S7
 def valid_rows(expert_num_tokens, M_max):
     ent = np.asarray(expert_num_tokens)
@@ -216,10 +240,11 @@ def valid_rows(expert_num_tokens, M_max):
                            for e, n in enumerate(ent)] + [np.zeros(0, np.int64)])
 
 
-def w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h=False):
+def w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h=False, row_expert=None):
     """w13 GEMM + SiLU-and-mul + requant for the given global rows.
 
     Returns (h, y_q, y_sf) as full-size arrays [E*M_max, .]; only `rows` are set.
+    row_expert: expert of each row (contiguous layout); None = row // M_max.
     """
     lib = _load()
     rows = _c(rows, np.int64)
@@ -232,8 +257,9 @@ def w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h=False):
     h = np.zeros((R, 2 * N), np.uint16) if want_h else None
     y_q = np.zeros((R, N), np.uint8)
     y_sf = np.zeros((R, (Gn + 3) // 4), np.int32)
+    re = None if row_expert is None else _c(row_expert, np.int64)
     lib.orc_w13_rows(rows.size, _p(rows), M_max, K, N, _p(x_b), _p(a_sf), _p(w13), _p(w13_s),
-                     _p(h), _p(y_q), _p(y_sf))
+                     _p(h), _p(y_q), _p(y_sf), _p(re))
     return h, y_q, y_sf
 
 
@@ -249,8 +275,11 @@ def silu_requant_rows(rows, N, h_bits):
     return y_q, y_sf
 
 
-def w2_rows(rows, M_max, K, N, y_q, y_sf, w2, w2_s):
-    """w2 GEMM for the given global rows; returns bf16 bits [E*M_max, K]."""
+def w2_rows(rows, M_max, K, N, y_q, y_sf, w2, w2_s, row_expert=None):
+    """w2 GEMM for the given global rows; returns bf16 bits [E*M_max, K].
+
+    row_expert: expert of each row (contiguous layout); None = row // M_max.
+    """
     lib = _load()
     rows = _c(rows, np.int64)
     y_q = _c(y_q, np.uint8)
@@ -258,19 +287,21 @@ def w2_rows(rows, M_max, K, N, y_q, y_sf, w2, w2_s):
     w2 = _c(w2, np.uint8)
     w2_s = _c(w2_s, np.float32)
     out_b = np.zeros((y_q.shape[0], K), np.uint16)
+    re = None if row_expert is None else _c(row_expert, np.int64)
     lib.orc_w2_rows(rows.size, _p(rows), M_max, K, N, _p(y_q), _p(y_sf), _p(w2), _p(w2_s),
-                    _p(out_b))
+                    _p(out_b), _p(re))
     return out_b
 
 
 # --------------------------------------------------------------------------- S8
 def topk_reduce(out_b_bits, ids, route_slot, weights, M_max):
+    """S8.  ids None: route_slot holds the rows (contiguous layout)."""
     lib = _load()
     out_b = _c(out_b_bits, np.uint16)
-    ids = _c(ids, np.int64)
+    ids = None if ids is None else _c(ids, np.int64)
     slot = _c(route_slot, np.int32)
     w = _c(weights, np.float32)
-    T, top_k = ids.shape
+    T, top_k = slot.shape
     K = out_b.shape[-1]
     out = np.zeros((T, K), np.uint16)
     lib.orc_topk_reduce(T, top_k, K, M_max, _p(out_b), _p(ids), _p(slot), _p(w), _p(out))

@@ -279,6 +279,42 @@ int orc_dispatch(int64_t T, int64_t top_k, int64_t K, const int64_t* ids, const 
 }
 
 /* ------------------------------------------------------------------------ */
+/* S6b: contiguous layout (HummingGroupedExperts.apply: moe_permute gives    */
+/* expert_offsets and the permuted rows).  Routes are visited in (token, k)  */
+/* order; the routes of expert e take rows offsets[e], offsets[e] + 1, ...  */
+/* where offsets[e] counts the routes to experts < e.  route_row[t, j] is    */
+/* the row (-1 when unrouted).  Returns 3 on an id >= E.                     */
+int orc_dispatch_contiguous(int64_t T, int64_t top_k, int64_t K, const int64_t* ids,
+                            const uint8_t* x, const int32_t* x_sf, int64_t E, int32_t* offsets,
+                            int32_t* expert_num_tokens, int32_t* route_row, uint8_t* x_c,
+                            int32_t* sf_c) {
+  const int64_t W = (K / 128 + 3) / 4;
+  int status = 0;
+  for (int64_t e = 0; e < E; ++e) expert_num_tokens[e] = 0;
+  for (int64_t r = 0; r < T * top_k; ++r) {
+    const int64_t id = ids[r];
+    if (id >= E) status = 3;
+    if (id >= 0 && id < E) expert_num_tokens[id] += 1;
+  }
+  offsets[0] = 0;
+  for (int64_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + expert_num_tokens[e];
+  int32_t* filled = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t j = 0; j < top_k; ++j) {
+      const int64_t id = ids[t * top_k + j];
+      route_row[t * top_k + j] = -1;
+      if (id < 0 || id >= E) continue;
+      const int64_t row = offsets[id] + filled[id];
+      filled[id] += 1;
+      route_row[t * top_k + j] = (int32_t)row;
+      if (x_c) memcpy(x_c + row * K, x + t * K, (size_t)K);
+      if (sf_c) memcpy(sf_c + row * W, x_sf + t * W, (size_t)W * sizeof(int32_t));
+    }
+  }
+  free(filled);
+  return status;
+}
+
 /* S7a: w13 GEMM + SiLU-and-mul + UE8M0 requant, for selected rows.          */
 /* rows       : n_rows global row indices r = e * M_max + m                  */
 /* x_b        : fp8 [E*M_max, K]; a_sf: packed UE8M0 words [E*M_max, ceil(G/4)]*/
@@ -313,16 +349,19 @@ static void silu_requant_row(const double* hb, int64_t N, uint8_t* yq_row, uint3
   free(y);
 }
 
+/* row_expert[i] (nullable): expert of rows[i]; NULL means rows[i] / M_max  */
+/* (batched layout).                                                         */
 void orc_w13_rows(int64_t n_rows, const int64_t* rows, int64_t M_max, int64_t K, int64_t N,
                   const uint8_t* x_b, const int32_t* a_sf, const uint8_t* w13,
-                  const float* w13_s, uint16_t* h_out, uint8_t* y_q, int32_t* y_sf) {
+                  const float* w13_s, uint16_t* h_out, uint8_t* y_q, int32_t* y_sf,
+                  const int64_t* row_expert) {
   const int64_t G = K / 128, Wa = (G + 3) / 4;
   const int64_t Gn = N / 128, Wy = (Gn + 3) / 4;
   const int64_t twoN = 2 * N;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < n_rows; ++i) {
     const int64_t r = rows[i];
-    const int64_t e = r / M_max;
+    const int64_t e = row_expert ? row_expert[i] : r / M_max;
     double* a = (double*)malloc(sizeof(double) * (size_t)K);
     double* hb = (double*)malloc(sizeof(double) * (size_t)twoN);
     for (int64_t k = 0; k < K; ++k)
@@ -360,12 +399,12 @@ void orc_silu_requant_rows(int64_t n_rows, const int64_t* rows, int64_t N, const
 /* S7b: w2 GEMM for selected rows: out_b[r, c] = bf16(sum_n deq(y) deq(w2)). */
 void orc_w2_rows(int64_t n_rows, const int64_t* rows, int64_t M_max, int64_t K, int64_t N,
                  const uint8_t* y_q, const int32_t* y_sf, const uint8_t* w2,
-                 const float* w2_s, uint16_t* out_b) {
+                 const float* w2_s, uint16_t* out_b, const int64_t* row_expert) {
   const int64_t Gn = N / 128, Wy = (Gn + 3) / 4;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < n_rows; ++i) {
     const int64_t r = rows[i];
-    const int64_t e = r / M_max;
+    const int64_t e = row_expert ? row_expert[i] : r / M_max;
     double* a = (double*)malloc(sizeof(double) * (size_t)N);
     for (int64_t n = 0; n < N; ++n)
       a[n] = (double)orc_e4m3_decode(y_q[r * N + n]) * a_scale_of(y_sf, Wy, r, n / 128);
@@ -394,10 +433,17 @@ void orc_topk_reduce(int64_t T, int64_t top_k, int64_t K, int64_t M_max, const u
     for (int64_t c = 0; c < K; ++c) {
       double acc = 0.0;
       for (int64_t j = 0; j < top_k; ++j) {
-        int64_t id = ids[t * top_k + j];
         int32_t s = route_slot[t * top_k + j];
-        if (id < 0 || s < 0) continue;
-        acc += (double)w[t * top_k + j] * (double)bf16_to_f32(out_b[(id * M_max + s) * K + c]);
+        int64_t row;
+        if (ids) {
+          int64_t id = ids[t * top_k + j];
+          if (id < 0 || s < 0) continue;
+          row = id * M_max + s;
+        } else {  /* contiguous layout (moe_unpermute): the slot is the row */
+          if (s < 0) continue;
+          row = s;
+        }
+        acc += (double)w[t * top_k + j] * (double)bf16_to_f32(out_b[row * K + c]);
       }
       out[t * K + c] = orc_bf16_from_f64(acc);
     }
