@@ -89,7 +89,7 @@ typedef enum moe_activation { MOE_ACT_SILU = 0 } moe_activation_t;
 /* logical_to_physical[l * map_stride + (t mod logical_replica_count[l])]    */
 /* and, when *should_record != 0 and t < *num_unpadded_tokens, adds 1 to     */
 /* expert_load[physical id].                                                 */
-/* Dispatch (when x_b != NULL; requires MOE_SF_UE8M0_PACKED): routes are     */
+/* Dispatch (when x_b != NULL; UE8M0 or FP32 scales): routes are            */
 /* placed in (token, k) order; route (t, j) with id e takes slot s, the      */
 /* number of earlier routes to e, and x_b[e, s, :] = x[t, :],                */
 /* sf_b[e, s, :] = x_sf[t, :], route_slot[t, j] = s (-1 when unrouted or     */
@@ -166,7 +166,7 @@ typedef struct moe_prepare_args {
   int64_t num_experts;           /* E */
   int64_t max_tokens_per_expert; /* M_max */
   void* x_b;                     /* fp8 [E, M_max, K] */
-  int32_t* sf_b;                 /* int32 [E, M_max, ceil(G/4)] */
+  void* sf_b;                    /* int32 [E, M_max, ceil(G/4)] packed UE8M0, or fp32 [E, M_max, G] */
   int32_t* expert_num_tokens;    /* int32 [E] */
   int32_t* route_slot;           /* int32 [T, k], contiguous */
   int32_t* expert_offsets;       /* nullable int32 [E + 1]: contiguous layout */
@@ -230,7 +230,10 @@ moe_status_t moe_prepare_inputs_noalloc(const moe_prepare_args_t* args, void* st
 /* slab in fp32.                                                              */
 /*                                                                           */
 /* Layouts: x_b [E*M_max, K] fp8, a_scale int32 [E*M_max, ceil(G/4)] packed  */
-/* UE8M0 (a_scale_mode MOE_SF_UE8M0_PACKED), w13 [E, 2N, K] fp8 K-major,     */
+/* UE8M0 (a_scale_mode MOE_SF_UE8M0_PACKED) or fp32 [E*M_max, G] with       */
+/* deq(x) = x * a_scale[row, k/128] (MOE_SF_FP32: the fp32 a1q_scale        */
+/* [M, K/128] contract of process_input / get_buffer_metas; the requantised */
+/* w2 input stays 1x128 UE8M0), w13 [E, 2N, K] fp8 K-major,                  */
 /* w13_scale fp32 [E, 2N/128, G], w2 [E, K, N] fp8 N-major, w2_scale fp32     */
 /* [E, K/128, Gn], output bf16 [E, M_max, K].  All contiguous.  Base pointers*/
 /* of x_b, w13, w2, inter_q must be 16-byte aligned.                          */
@@ -246,8 +249,8 @@ moe_status_t moe_prepare_inputs_noalloc(const moe_prepare_args_t* args, void* st
 /* workspace2 holds split-K partials and tile counters.  It must be zero-    */
 /* filled once when allocated; every call leaves its counters at zero again   */
 /* (after a MOE_DEV_TIMEOUT, zero it before reuse).                           */
-/* Errors: K % 128, N % 128 -> SHAPE; activation != SILU, a_scale_mode !=    */
-/* UE8M0_PACKED -> UNSUPPORTED; short workspaces -> WORKSPACE.               */
+/* Errors: K % 128, N % 128 -> SHAPE; activation != SILU, a_scale_mode not   */
+/* UE8M0_PACKED or FP32 -> UNSUPPORTED; short workspaces -> WORKSPACE.       */
 /* ------------------------------------------------------------------------ */
 typedef struct moe_experts_args {
   int64_t num_experts;           /* E */

@@ -271,7 +271,9 @@ def moe_batched_experts(output, hidden, a_scale, w13, w13_scale, w2, w2_scale,
     a.num_experts, a.max_tokens_per_expert, a.hidden_size, a.intermediate_size = E, M_max, K, N
     a.activation, a.stages = MOE_ACT_SILU, stages
     a.output, a.hidden, a.a_scale = _ptr(output), _ptr(hidden), _ptr(a_scale)
-    a.a_scale_mode = MOE_SF_UE8M0_PACKED
+    # fp32 activation scales [E*M_max, K/128] select the fp32 dequantisation
+    a.a_scale_mode = (MOE_SF_FP32 if a_scale is not None and a_scale.dtype == torch.float32
+                      else MOE_SF_UE8M0_PACKED)
     a.w13, a.w13_scale, a.w2, a.w2_scale = _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale)
     a.expert_num_tokens = _ptr(expert_num_tokens)
     a.expert_offsets = _ptr(expert_offsets)
@@ -311,12 +313,15 @@ class MoeLayer:
     """
 
     def __init__(self, T, K, N, E, top_k, M_max, w13, w13_s, w2, w2_s, device="cuda",
-                 valid_shape_m=None, eplb=None, contiguous=False):
+                 valid_shape_m=None, eplb=None, contiguous=False, fp32_scales=False):
         # contiguous: rows are packed per expert (expert_offsets); the buffers
         # hold E * ceil(T*k/E) rows, whatever the per-expert load
         if contiguous:
             M_max = max(1, -(-(T * top_k) // E))
         self.contiguous = contiguous
+        # fp32_scales: 1x128 activation scales kept as fp32 (amax / 448) instead
+        # of packed UE8M0 exponents
+        self.sf_mode = MOE_SF_FP32 if fp32_scales else MOE_SF_UE8M0_PACKED
         self.T, self.K, self.N, self.E, self.top_k, self.M_max = T, K, N, E, top_k, M_max
         self.w13, self.w13_s, self.w2, self.w2_s = w13, w13_s, w2, w2_s
         self.eplb = eplb
@@ -325,11 +330,13 @@ class MoeLayer:
         dev = torch.device(device)
         u8 = dict(dtype=torch.uint8, device=dev)
         self.x = torch.empty((T, K), **u8)
-        self.x_sf = torch.empty((T, W), dtype=torch.int32, device=dev)
+        self.x_sf = (torch.empty((T, G), dtype=torch.float32, device=dev) if fp32_scales else
+                     torch.empty((T, W), dtype=torch.int32, device=dev))
         self.ids_out = torch.empty((T, top_k), dtype=torch.int64, device=dev)
         self.w_out = torch.empty((T, top_k), dtype=torch.float32, device=dev)
         self.x_b = torch.empty((E * M_max, K), **u8)
-        self.sf_b = torch.empty((E * M_max, W), dtype=torch.int32, device=dev)
+        self.sf_b = (torch.empty((E * M_max, G), dtype=torch.float32, device=dev) if fp32_scales
+                     else torch.empty((E * M_max, W), dtype=torch.int32, device=dev))
         self.expert_num_tokens = torch.zeros(E, dtype=torch.int32, device=dev)
         self.route_slot = torch.empty((T, top_k), dtype=torch.int32, device=dev)
         self.expert_offsets = (torch.zeros(E + 1, dtype=torch.int32, device=dev) if contiguous
@@ -351,9 +358,9 @@ class MoeLayer:
 
     def prepare(self, hidden, topk_ids, topk_weights, is_padding=None, stream=None):
         moe_prepare_inputs(hidden, topk_ids, topk_weights, self.x, self.x_sf, self.ids_out,
-                           self.w_out, is_padding=is_padding, eplb=self.eplb,
-                           dispatch=self.dispatch_args(), device_status=self.status,
-                           stream=stream)
+                           self.w_out, is_padding=is_padding, sf_mode=self.sf_mode,
+                           eplb=self.eplb, dispatch=self.dispatch_args(),
+                           device_status=self.status, stream=stream)
 
     def experts(self, gate_up_dump=None, stream=None):
         moe_batched_experts(self.out_b, self.x_b, self.sf_b, self.w13, self.w13_s, self.w2,

@@ -133,8 +133,8 @@ moe_status_t moe_prepare_inputs(const moe_prepare_args_t* a, void* stream) {
       return set_error(MOE_ERR_INVALID_ARGUMENT, "expert_load needs num_physical > 0");
   }
   if (a->x_b != nullptr) {
-    if (a->sf_mode != MOE_SF_UE8M0_PACKED)
-      return set_error(MOE_ERR_UNSUPPORTED, "dispatch requires MOE_SF_UE8M0_PACKED scales");
+    if (a->sf_mode == MOE_SF_NONE)
+      return set_error(MOE_ERR_UNSUPPORTED, "dispatch requires quantised (UE8M0 or fp32) scales");
     if (a->num_experts <= 0 || a->num_experts > 1024 || a->max_tokens_per_expert <= 0)
       return set_error(MOE_ERR_SHAPE, "dispatch needs 0 < num_experts <= 1024, M_max > 0");
     if (!a->sf_b || !a->expert_num_tokens || !a->route_slot)
@@ -178,7 +178,7 @@ moe_status_t moe_batched_experts(const moe_experts_args_t* a, void* stream) {
     return set_error(MOE_ERR_SHAPE, "hidden_size and intermediate_size must be multiples of 128");
   if (a->activation != MOE_ACT_SILU)
     return set_error(MOE_ERR_UNSUPPORTED, "only SiLU-and-mul is implemented");
-  if (a->a_scale_mode != MOE_SF_UE8M0_PACKED)
+  if (a->a_scale_mode != MOE_SF_UE8M0_PACKED && a->a_scale_mode != MOE_SF_FP32)
     return set_error(MOE_ERR_UNSUPPORTED, "activation scales must be packed UE8M0");
   const int stages = a->stages == 0 ? MOE_STAGE_ALL : a->stages;
   if (stages < 1 || stages > 3) return set_error(MOE_ERR_INVALID_ARGUMENT, "bad stages mask");

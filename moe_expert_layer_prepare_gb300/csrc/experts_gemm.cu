@@ -75,8 +75,8 @@ struct GemmParams {
   int b_rows;      // rows of one expert in the B tensor (2N or K)
   const int32_t* expert_num_tokens;
   const int32_t* offsets;  // contiguous layout: [E+1] first row of each expert (nullable)
-  const uint32_t* a_sf;  // packed UE8M0 words [E*M_max, Wa]
-  int Wa;
+  const uint32_t* a_sf;  // packed UE8M0 words [E*M_max, Wa]; fp32 [E*M_max, Wa] when AF32
+  int Wa;                // row stride of a_sf in 4-byte words
   const float* w_s;      // [E, b_rows/128, KB]
   // w13 outputs
   uint8_t* y_q;          // [E*M_max, N]
@@ -302,7 +302,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const int* pref
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool W13>
+template <bool W13, bool AF32 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p,
                         const __grid_constant__ CUtensorMap tmA,
@@ -569,13 +569,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float wu_cur = wb + lane < w.kb1 ? __ldg(ws1 + wb + lane) : 0.0f;
       float wg_nxt = wb + 32 + lane < w.kb1 ? __ldg(ws0 + wb + 32 + lane) : 0.0f;
       float wu_nxt = wb + 32 + lane < w.kb1 ? __ldg(ws1 + wb + 32 + lane) : 0.0f;
-      uint32_t aw = row_ok ? __ldg(asf_row + (w.kb0 >> 2)) : 0x7F7F7F7Fu;
-      uint32_t aw_next = (row_ok && ((w.kb0 >> 2) + 1) * 4 < w.kb1)
-                             ? __ldg(asf_row + (w.kb0 >> 2) + 1) : 0x7F7F7F7Fu;
+      // UE8M0: packed exponent words; fp32 (AF32): a ring of the next four
+      // slabs' scales of this row
+      uint32_t aw = 0x7F7F7F7Fu, aw_next = 0x7F7F7F7Fu;
+      float af0 = 1.0f, af1 = 1.0f, af2 = 1.0f, af3 = 1.0f;
+      if constexpr (AF32) {
+        const float* afr = reinterpret_cast<const float*>(asf_row);
+        if (row_ok) {
+          af0 = __ldg(afr + w.kb0);
+          if (w.kb0 + 1 < w.kb1) af1 = __ldg(afr + w.kb0 + 1);
+          if (w.kb0 + 2 < w.kb1) af2 = __ldg(afr + w.kb0 + 2);
+          if (w.kb0 + 3 < w.kb1) af3 = __ldg(afr + w.kb0 + 3);
+        }
+      } else {
+        aw = row_ok ? __ldg(asf_row + (w.kb0 >> 2)) : 0x7F7F7F7Fu;
+        aw_next = (row_ok && ((w.kb0 >> 2) + 1) * 4 < w.kb1) ? __ldg(asf_row + (w.kb0 >> 2) + 1)
+                                                              : 0x7F7F7F7Fu;
+      }
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        if (kb > w.kb0 && (kb & 3) == 0) {
-          aw = aw_next;
-          if (row_ok && ((kb >> 2) + 1) * 4 < w.kb1) aw_next = __ldg(asf_row + (kb >> 2) + 1);
+        if constexpr (!AF32) {
+          if (kb > w.kb0 && (kb & 3) == 0) {
+            aw = aw_next;
+            if (row_ok && ((kb >> 2) + 1) * 4 < w.kb1) aw_next = __ldg(asf_row + (kb >> 2) + 1);
+          }
         }
         if (kb - wb == 32) {
           wb = kb;
@@ -584,8 +600,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           wg_nxt = wb + 32 + lane < w.kb1 ? __ldg(ws0 + wb + 32 + lane) : 0.0f;
           wu_nxt = wb + 32 + lane < w.kb1 ? __ldg(ws1 + wb + 32 + lane) : 0.0f;
         }
-        const uint32_t ea = (aw >> (8 * (kb & 3))) & 0xFFu;
-        const float sa = __uint_as_float(max(ea, 1u) << 23);
+        float sa;
+        if constexpr (AF32) {
+          sa = af0;
+          af0 = af1;
+          af1 = af2;
+          af2 = af3;
+          if (row_ok && kb + 4 < w.kb1)
+            af3 = __ldg(reinterpret_cast<const float*>(asf_row) + kb + 4);
+        } else {
+          const uint32_t ea = (aw >> (8 * (kb & 3))) & 0xFFu;
+          sa = __uint_as_float(max(ea, 1u) << 23);
+        }
         const float s0 = sa * __shfl_sync(0xFFFFFFFFu, wg_cur, kb - wb);
         const float s1 = sa * __shfl_sync(0xFFFFFFFFu, wu_cur, kb - wb);
         // warp-uniform outcome; also reconverges the warp before the
@@ -898,18 +924,23 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     cudaError_t e2 = cudaFuncSetAttribute(moe::grouped_gemm_kernel<false>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e1 != cudaSuccess || e2 != cudaSuccess)
+    cudaError_t e3 = cudaFuncSetAttribute(moe::grouped_gemm_kernel<true, true>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "GEMM smem attribute: %s",
-                       cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+                       cudaGetErrorString(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3)));
     // The in-kernel register split assumes the launch allocation below.
-    cudaFuncAttributes fa13, fa2;
+    cudaFuncAttributes fa13, fa2, fa13f;
     if (cudaFuncGetAttributes(&fa13, moe::grouped_gemm_kernel<true>) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa2, moe::grouped_gemm_kernel<false>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa2, moe::grouped_gemm_kernel<false>) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa13f, moe::grouped_gemm_kernel<true, true>) != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "cudaFuncGetAttributes failed for the GEMM kernels");
-    if (fa13.numRegs != moe::LAUNCH_REGS || fa2.numRegs != moe::LAUNCH_REGS)
+    if (fa13.numRegs != moe::LAUNCH_REGS || fa2.numRegs != moe::LAUNCH_REGS ||
+        fa13f.numRegs != moe::LAUNCH_REGS)
       return set_error(MOE_ERR_UNSUPPORTED,
-                       "GEMM kernels built with %d/%d registers per thread; the register "
-                       "split needs exactly %d", fa13.numRegs, fa2.numRegs, moe::LAUNCH_REGS);
+                       "GEMM kernels built with %d/%d/%d registers per thread; the register "
+                       "split needs exactly %d", fa13.numRegs, fa2.numRegs, fa13f.numRegs,
+                       moe::LAUNCH_REGS);
     attr_done[0] = true;
   }
   // Upper bound of the work units: every expert full.  Persistent grid.
@@ -930,7 +961,8 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
     p.expert_num_tokens = a->expert_num_tokens;
     p.offsets = a->expert_offsets;
     p.a_sf = static_cast<const uint32_t*>(a->a_scale);
-    p.Wa = (int)((K / 128 + 3) / 4);
+    const bool af32 = a->a_scale_mode == MOE_SF_FP32;
+    p.Wa = af32 ? (int)(K / 128) : (int)((K / 128 + 3) / 4);
     p.w_s = a->w13_scale;
     p.y_q = inter_q;
     p.y_sf_bytes = reinterpret_cast<uint8_t*>(inter_sf);
@@ -948,8 +980,11 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
       return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the w13 operands");
     const int64_t units = mt_cap * p.n_tiles;
     const int grid = (int)(units < sms ? (units < 1 ? 1 : units) : sms);
-    cudaError_t e = launch_pdl(moe::grouped_gemm_kernel<true>, dim3(grid), dim3(moe::NUM_THREADS),
-                               smem, s, p, tA, tB);
+    cudaError_t e =
+        af32 ? launch_pdl(moe::grouped_gemm_kernel<true, true>, dim3(grid),
+                          dim3(moe::NUM_THREADS), smem, s, p, tA, tB)
+             : launch_pdl(moe::grouped_gemm_kernel<true>, dim3(grid), dim3(moe::NUM_THREADS),
+                          smem, s, p, tA, tB);
     if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "w13 launch: %s", cudaGetErrorString(e));
   }
   if (stages & MOE_STAGE_W2) {

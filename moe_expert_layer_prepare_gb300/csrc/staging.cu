@@ -57,7 +57,7 @@ struct StageParams {
   // dispatch
   int64_t E, M_max;
   uint8_t* x_b;
-  int32_t* sf_b;
+  int32_t* sf_b;        // packed UE8M0 words [rows, W], or fp32 [rows, G] (FP32 mode)
   int32_t* expert_num_tokens;
   int32_t* route_slot;
   int32_t* offsets;     // contiguous layout: [E+1] first row of each expert (nullable)
@@ -348,7 +348,15 @@ __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int6
           uint8_t* brow = p.x_b + row * K;
           if (actA) st_v2(brow + offA, qA);
           if (actB) st_v2(brow + offB, qB);
-          if (lane == 0) p.sf_b[row * p.W + w] = (int32_t)word;
+          if constexpr (SF_MODE == MOE_SF_UE8M0_PACKED) {
+            if (lane == 0) p.sf_b[row * p.W + w] = (int32_t)word;
+          } else {  // fp32 scales [rows, G]
+            if ((lane & 15) == 0) {
+              float* sfb = reinterpret_cast<float*>(p.sf_b) + row * p.G;
+              if (actA) sfb[gA] = __uint_as_float(cA);
+              if (actB) sfb[gB] = __uint_as_float(cB);
+            }
+          }
         }
         if (w == 0 && lane == 0) p.route_slot[r] = (int32_t)slot;
       }
@@ -520,9 +528,11 @@ static moe_status_t launch_typed(StageParams& p, bool dispatch, int sf_mode, cud
       return set_error(MOE_ERR_CUDA, "route_kernel launch: %s", cudaGetErrorString(le));
     // the shared-expert pages are a separate instantiation: even untaken,
     // their code costs the streaming loop ~10%
-    auto qk = p.shared_sf != nullptr
-                  ? moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, true>
-                  : moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, false>;
+    auto qk = sf_mode == MOE_SF_FP32
+                  ? moe::quant_kernel<MOE_SF_FP32, false, true, IdT, WT, false>
+                  : (p.shared_sf != nullptr
+                         ? moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, true>
+                         : moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, false>);
     le = launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
     if (le != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "quant_kernel launch: %s", cudaGetErrorString(le));
@@ -599,7 +609,7 @@ moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s) {
     p.E = a->num_experts;
     p.M_max = a->max_tokens_per_expert;
     p.x_b = static_cast<uint8_t*>(a->x_b);
-    p.sf_b = a->sf_b;
+    p.sf_b = static_cast<int32_t*>(a->sf_b);
     p.expert_num_tokens = a->expert_num_tokens;
     p.route_slot = a->route_slot;
     p.offsets = a->expert_offsets;

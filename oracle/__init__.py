@@ -75,11 +75,12 @@ def _load():
         lib.orc_shared_sf.restype = None
         lib.orc_shared_sf.argtypes = [i64, i64, vp, i64, vp, i64, i64]
         lib.orc_dispatch_contiguous.restype = i32
-        lib.orc_dispatch_contiguous.argtypes = [i64, i64, i64, vp, vp, vp, i64, vp, vp, vp, vp, vp]
+        lib.orc_dispatch_contiguous.argtypes = [i64, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp,
+                                                vp, vp]
         lib.orc_dispatch.restype = i32
-        lib.orc_dispatch.argtypes = [i64, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, vp]
+        lib.orc_dispatch.argtypes = [i64, i64, i64, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
         lib.orc_w13_rows.restype = None
-        lib.orc_w13_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_w13_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, i32]
         lib.orc_silu_requant_rows.restype = None
         lib.orc_silu_requant_rows.argtypes = [i64, vp, i64, vp, vp, vp]
         lib.orc_w2_rows.restype = None
@@ -92,6 +93,14 @@ def _load():
 
 def _p(a):
     return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _sf_words(a):
+    """Scale rows as 4-byte words: packed UE8M0 int32 as is, fp32 bit patterns."""
+    a = np.asarray(a)
+    if a.dtype == np.float32:
+        return np.ascontiguousarray(a).view(np.int32)
+    return _c(a, np.int32)
 
 
 def _c(a, dtype):
@@ -200,14 +209,16 @@ def dispatch(ids, x, x_sf_words, E, M_max, copy_rows=True):
     T, top_k = ids.shape
     x = _c(x, np.uint8)
     K = x.shape[1]
-    sfw = _c(x_sf_words, np.int32)
+    sfw = _sf_words(x_sf_words)
     W = sfw.shape[1]
     ent = np.zeros(E, np.int32)
     slot = np.zeros((T, top_k), np.int32)
     x_b = np.zeros((E * M_max, K), np.uint8) if copy_rows else None
     sf_b = np.zeros((E * M_max, W), np.int32) if copy_rows else None
-    st = lib.orc_dispatch(T, top_k, K, _p(ids), _p(x), _p(sfw), E, M_max, _p(ent), _p(slot),
+    st = lib.orc_dispatch(T, top_k, K, _p(ids), _p(x), _p(sfw), W, E, M_max, _p(ent), _p(slot),
                           _p(x_b), _p(sf_b))
+    if sf_b is not None and np.asarray(x_sf_words).dtype == np.float32:
+        sf_b = sf_b.view(np.float32)
     return dict(expert_num_tokens=ent, route_slot=slot, x_b=x_b, sf_b=sf_b, status=int(st))
 
 
@@ -219,15 +230,17 @@ def dispatch_contiguous(ids, x, x_sf_words, E):
     T, top_k = ids.shape
     x = _c(x, np.uint8)
     K = x.shape[1]
-    sfw = _c(x_sf_words, np.int32)
+    sfw = _sf_words(x_sf_words)
     W = sfw.shape[1]
     offs = np.zeros(E + 1, np.int32)
     ent = np.zeros(E, np.int32)
     row = np.zeros((T, top_k), np.int32)
     x_c = np.zeros((max(T * top_k, 1), K), np.uint8)
     sf_c = np.zeros((max(T * top_k, 1), W), np.int32)
-    st = lib.orc_dispatch_contiguous(T, top_k, K, _p(ids), _p(x), _p(sfw), E, _p(offs), _p(ent),
-                                     _p(row), _p(x_c), _p(sf_c))
+    st = lib.orc_dispatch_contiguous(T, top_k, K, _p(ids), _p(x), _p(sfw), W, E, _p(offs),
+                                     _p(ent), _p(row), _p(x_c), _p(sf_c))
+    if np.asarray(x_sf_words).dtype == np.float32:
+        sf_c = sf_c.view(np.float32)
     row_expert = np.repeat(np.arange(E, dtype=np.int64), ent)
     return dict(expert_offsets=offs, expert_num_tokens=ent, route_row=row, x_c=x_c, sf_c=sf_c,
                 row_expert=row_expert, status=int(st))
@@ -241,6 +254,11 @@ def valid_rows(expert_num_tokens, M_max):
 
 
 def w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h=False, row_expert=None):
+    """(a_sf: packed UE8M0 int32 words, or fp32 scales [rows, K/128])"""
+    return _w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h, row_expert)
+
+
+def _w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h, row_expert):
     """w13 GEMM + SiLU-and-mul + requant for the given global rows.
 
     Returns (h, y_q, y_sf) as full-size arrays [E*M_max, .]; only `rows` are set.
@@ -250,7 +268,8 @@ def w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h=False, row_expert=
     rows = _c(rows, np.int64)
     x_b = _c(x_b, np.uint8)
     R = x_b.shape[0]
-    a_sf = _c(a_sf, np.int32)
+    a_fp32 = int(np.asarray(a_sf).dtype == np.float32)
+    a_sf = _sf_words(a_sf)
     w13 = _c(w13, np.uint8)
     w13_s = _c(w13_s, np.float32)
     Gn = N // 128
@@ -259,7 +278,7 @@ def w13_rows(rows, M_max, K, N, x_b, a_sf, w13, w13_s, want_h=False, row_expert=
     y_sf = np.zeros((R, (Gn + 3) // 4), np.int32)
     re = None if row_expert is None else _c(row_expert, np.int64)
     lib.orc_w13_rows(rows.size, _p(rows), M_max, K, N, _p(x_b), _p(a_sf), _p(w13), _p(w13_s),
-                     _p(h), _p(y_q), _p(y_sf), _p(re))
+                     _p(h), _p(y_q), _p(y_sf), _p(re), a_fp32)
     return h, y_q, y_sf
 
 

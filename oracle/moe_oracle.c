@@ -254,10 +254,10 @@ void orc_shared_sf(int64_t T, int64_t G, const int32_t* x_sf_words, int64_t bloc
 /* whose expert is full is not placed (route_slot = -1) and the function     */
 /* returns 1 (capacity).  sf rows are packed UE8M0 words [., ceil(G/4)].     */
 /* ------------------------------------------------------------------------ */
+/* W: 4-byte words per scale row (packed UE8M0 words, or fp32 scales).     */
 int orc_dispatch(int64_t T, int64_t top_k, int64_t K, const int64_t* ids, const uint8_t* x,
-                 const int32_t* x_sf, int64_t E, int64_t M_max, int32_t* expert_num_tokens,
-                 int32_t* route_slot, uint8_t* x_b, int32_t* sf_b) {
-  const int64_t W = (K / 128 + 3) / 4;
+                 const int32_t* x_sf, int64_t W, int64_t E, int64_t M_max,
+                 int32_t* expert_num_tokens, int32_t* route_slot, uint8_t* x_b, int32_t* sf_b) {
   int status = 0;
   for (int64_t e = 0; e < E; ++e) expert_num_tokens[e] = 0;
   for (int64_t t = 0; t < T; ++t) {
@@ -285,10 +285,9 @@ int orc_dispatch(int64_t T, int64_t top_k, int64_t K, const int64_t* ids, const 
 /* where offsets[e] counts the routes to experts < e.  route_row[t, j] is    */
 /* the row (-1 when unrouted).  Returns 3 on an id >= E.                     */
 int orc_dispatch_contiguous(int64_t T, int64_t top_k, int64_t K, const int64_t* ids,
-                            const uint8_t* x, const int32_t* x_sf, int64_t E, int32_t* offsets,
-                            int32_t* expert_num_tokens, int32_t* route_row, uint8_t* x_c,
-                            int32_t* sf_c) {
-  const int64_t W = (K / 128 + 3) / 4;
+                            const uint8_t* x, const int32_t* x_sf, int64_t W, int64_t E,
+                            int32_t* offsets, int32_t* expert_num_tokens, int32_t* route_row,
+                            uint8_t* x_c, int32_t* sf_c) {
   int status = 0;
   for (int64_t e = 0; e < E; ++e) expert_num_tokens[e] = 0;
   for (int64_t r = 0; r < T * top_k; ++r) {
@@ -354,7 +353,7 @@ static void silu_requant_row(const double* hb, int64_t N, uint8_t* yq_row, uint3
 void orc_w13_rows(int64_t n_rows, const int64_t* rows, int64_t M_max, int64_t K, int64_t N,
                   const uint8_t* x_b, const int32_t* a_sf, const uint8_t* w13,
                   const float* w13_s, uint16_t* h_out, uint8_t* y_q, int32_t* y_sf,
-                  const int64_t* row_expert) {
+                  const int64_t* row_expert, int a_sf_fp32) {
   const int64_t G = K / 128, Wa = (G + 3) / 4;
   const int64_t Gn = N / 128, Wy = (Gn + 3) / 4;
   const int64_t twoN = 2 * N;
@@ -365,7 +364,9 @@ void orc_w13_rows(int64_t n_rows, const int64_t* rows, int64_t M_max, int64_t K,
     double* a = (double*)malloc(sizeof(double) * (size_t)K);
     double* hb = (double*)malloc(sizeof(double) * (size_t)twoN);
     for (int64_t k = 0; k < K; ++k)
-      a[k] = (double)orc_e4m3_decode(x_b[r * K + k]) * a_scale_of(a_sf, Wa, r, k / 128);
+      a[k] = (double)orc_e4m3_decode(x_b[r * K + k]) *
+             (a_sf_fp32 ? (double)((const float*)a_sf)[r * G + k / 128]
+                        : a_scale_of(a_sf, Wa, r, k / 128));
     for (int64_t j = 0; j < twoN; ++j) {
       const uint8_t* wrow = w13 + (e * twoN + j) * K;
       const float* srow = w13_s + (e * (twoN / 128) + j / 128) * G;

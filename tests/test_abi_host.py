@@ -82,8 +82,10 @@ def test_prepare_rejects(lib):
              max_tokens_per_expert=8, workspace=FAKE, workspace_bytes=16)
     st, msg = _prep(lib, _prep_args(**d))
     assert st == 5 and "workspace" in msg
-    st, _ = _prep(lib, _prep_args(sf_mode=B.MOE_SF_FP32, **d))
-    assert st == 3
+    st, _ = _prep(lib, _prep_args(sf_mode=B.MOE_SF_NONE, x_sf=None, **d))
+    assert st == 3  # dispatch needs quantised scales (UE8M0 or fp32)
+    st, msg = _prep(lib, _prep_args(sf_mode=B.MOE_SF_FP32, **d))
+    assert st == 5 and "workspace" in msg  # fp32 scales pass the mode check
     st, _ = _prep(lib, _prep_args(num_experts=2000, **{k: v for k, v in d.items()
                                                          if k != "num_experts"}))
     assert st == 2
@@ -124,7 +126,8 @@ def test_experts_rejects(lib):
     assert run(_exp_args(hidden_size=200)) == 2
     assert run(_exp_args(intermediate_size=100)) == 2
     assert run(_exp_args(activation=3)) == 3
-    assert run(_exp_args(a_scale_mode=B.MOE_SF_FP32)) == 3
+    assert run(_exp_args(a_scale_mode=B.MOE_SF_NONE)) == 3
+    assert run(_exp_args(a_scale_mode=B.MOE_SF_FP32)) == 5  # fp32 scales accepted
     assert run(_exp_args(stages=B.MOE_STAGE_W2)) == 1     # w2 alone needs inter_q/inter_sf
     assert run(_exp_args(w13=FAKE + 4)) == 4
     assert run(_exp_args()) == 5                          # workspace13 too small

@@ -246,3 +246,32 @@ def test_brute_force_detects_planted_mistakes(orc, mistake):
     a = _bf16_vals(base).astype(np.float64)
     b = _bf16_vals(bad).astype(np.float64)
     assert np.linalg.norm(a - b) > 0.05 * np.linalg.norm(a)
+
+
+def test_fp32_activation_scales_match_ue8m0_when_powers_of_two(orc):
+    """The fp32 a1q_scale path dequantises with the fp32 scale itself; fed
+    the UE8M0 scales 2^(e-127) as fp32 it must reproduce the packed-exponent
+    rows bit for bit (the two modes differ only in how the scale is held)."""
+    from moe_expert_layer_prepare_gb300 import synthetic as syn
+    from tests._util import bf16_bits
+    T, K, N, E = 12, 384, 256, 2
+    hid = syn.make_hidden(T, K, 77, outlier_frac=0.05)
+    st = orc.prepare_inputs(bf16_bits(hid), np.zeros((T, 1), np.int32),
+                            np.ones((T, 1), np.float32))
+    words = st["x_sf"]
+    G = K // 128
+    exps = np.array([[(int(words[t, g // 4]) >> (8 * (g % 4))) & 0xFF for g in range(G)]
+                     for t in range(T)], np.uint32)
+    scales = (exps << 23).view(np.float32)  # 2^(e - 127)
+    w13, w13_s = syn.make_block_fp8_weights(E, 2 * N, K, 78)
+    rows = np.arange(T)
+    packed = orc.w13_rows(rows, T, K, N, st["x"], words, w13.numpy(), w13_s.numpy(), want_h=True)
+    fp32 = orc.w13_rows(rows, T, K, N, st["x"], scales, w13.numpy(), w13_s.numpy(), want_h=True)
+    for a, b in zip(packed, fp32):
+        assert np.array_equal(a, b)
+    # a scale that is not a power of two changes the result in proportion
+    scaled = orc.w13_rows(rows, T, K, N, st["x"], scales * np.float32(1.5), w13.numpy(),
+                          w13_s.numpy(), want_h=True)
+    from tests._util import bf16_vals
+    h1, h15 = bf16_vals(packed[0]).astype(np.float64), bf16_vals(scaled[0]).astype(np.float64)
+    assert np.all(np.abs(h15 - 1.5 * h1) <= 2.0 ** -7 * np.abs(1.5 * h1) + 1e-30)
