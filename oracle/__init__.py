@@ -70,6 +70,12 @@ def _load():
         lib.orc_prepare_inputs.restype = i32
         lib.orc_prepare_inputs.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32, vp, vp,
                                            vp, vp, vp, i64, i64, vp, vp, i64, i32, i64]
+        lib.orc_e2m1_encode.restype = ctypes.c_uint8
+        lib.orc_e2m1_encode.argtypes = [f32]
+        lib.orc_e2m1_decode.restype = f32
+        lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_nvfp4_rows.restype = None
+        lib.orc_nvfp4_rows.argtypes = [i64, i64, vp, vp, vp, vp]
         lib.orc_shared_sf_row.restype = i64
         lib.orc_shared_sf_row.argtypes = [i64, i64]
         lib.orc_shared_sf.restype = None
@@ -180,6 +186,27 @@ def prepare_inputs(hidden_bf16_bits, topk_ids, topk_weights, is_padding=None, sf
 
 
 # --------------------------------------------------------------------------- S6
+def e2m1_encode(v: float) -> int:
+    return int(_load().orc_e2m1_encode(float(v)))
+
+
+def e2m1_decode(code: int) -> float:
+    return float(_load().orc_e2m1_decode(int(code)))
+
+
+def nvfp4_rows(hidden_bf16_bits):
+    """NVFP4 staging of token rows (N2).  Returns dict(x [T, K/2] uint8,
+    x_sf [T, K/64] int32 of packed E4M3 block scales, x_scales [T] fp32)."""
+    lib = _load()
+    hidden = _c(hidden_bf16_bits, np.uint16)
+    T, K = hidden.shape
+    x = np.zeros((T, K // 2), np.uint8)
+    x_sf = np.zeros((T, (K // 16 + 3) // 4), np.int32)
+    xs = np.zeros(T, np.float32)
+    lib.orc_nvfp4_rows(T, K, _p(hidden), _p(x), _p(x_sf), _p(xs))
+    return dict(x=x, x_sf=x_sf, x_scales=xs)
+
+
 def shared_sf_row(t: int, block_m: int) -> int:
     """Row of token t in the shared-expert scale pages (S4b)."""
     return int(_load().orc_shared_sf_row(int(t), int(block_m)))

@@ -249,6 +249,86 @@ void orc_shared_sf(int64_t T, int64_t G, const int32_t* x_sf_words, int64_t bloc
   }
 }
 
+/* ------------------------------------------------------------------------ */
+/* N1: FP4 E2M1 (OCP MX "E2M1": 1 sign, 2 exponent (bias 1), 1 mantissa    */
+/* bit; no infinities or NaN).  Magnitudes of codes 0..7:                    */
+/*   0, 0.5 (subnormal), 1, 1.5, 2, 3, 4, 6.                                 */
+float orc_e2m1_decode(uint8_t code) {
+  const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return (float)(sign ? -mag : mag);
+}
+
+/* Round to nearest, ties to the even code, saturate finite overflow to 6. */
+uint8_t orc_e2m1_encode(float v) {
+  const uint8_t sign = signbit(v) ? 0x8 : 0;
+  const double a = fabs((double)v);
+  if (a >= 6.0) return sign | 0x7;
+  int c = 0;                                     /* largest code with val <= a */
+  while (c < 7 && (double)orc_e2m1_decode((uint8_t)(c + 1)) <= a) ++c;
+  const double below = orc_e2m1_decode((uint8_t)c);
+  if (below == a) return sign | (uint8_t)c;
+  const double above = orc_e2m1_decode((uint8_t)(c + 1));
+  const double d_lo = a - below, d_hi = above - a;
+  int pick;
+  if (d_lo < d_hi) pick = c;
+  else if (d_hi < d_lo) pick = c + 1;
+  else pick = (c % 2 == 0) ? c : c + 1;
+  return sign | (uint8_t)pick;
+}
+
+/* N2: NVFP4 staging of one token row (prepare_megamoe_nvfp4_inputs,         */
+/* kNvfp4DynamicToken): the row is scaled by its own fp32 x_scale = amax /   */
+/* 2688 (2688 = 448 * 6, the largest E4M3 scale times the largest E2M1      */
+/* value) and quantised to E2M1 with one E4M3 scale per 16 values.  Reading */
+/* (the kernel body is not on the pages), in fp32 with IEEE roundings:       */
+/*   xs = amax / 2688;  inv = 1 / xs;  v_i = x_i * inv   (|v| <= 2688)       */
+/*   per 16 values: s = e4m3(max|v_i| / 6);  q_i = e2m1(v_i * (1 / dec(s)))  */
+/* amax == 0 gives xs = 0 and zero codes; a block whose scale rounds to 0    */
+/* gives zero codes.  Codes are packed two per byte (value 2i in the low    */
+/* nibble), scales four per int32 (block b in byte b % 4 of word b / 4).     */
+void orc_nvfp4_row(int64_t K, const uint16_t* hidden_row, uint8_t* x_row, int32_t* sf_row,
+                   float* x_scale) {
+  if (K <= 0) return;
+  const int64_t nb = K / 16;
+  float amax = 0.0f;
+  for (int64_t i = 0; i < K; ++i) {
+    const float a = fabsf(bf16_to_f32(hidden_row[i]));
+    if (a > amax) amax = a;
+  }
+  const float xs = amax / 2688.0f;
+  *x_scale = xs;
+  memset(x_row, 0, (size_t)K / 2);
+  memset(sf_row, 0, ((size_t)nb + 3) / 4 * 4);
+  if (amax == 0.0f) return;
+  const float inv = 1.0f / xs;
+  for (int64_t b = 0; b < nb; ++b) {
+    float v[16], bmax = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      v[i] = bf16_to_f32(hidden_row[b * 16 + i]) * inv;
+      if (fabsf(v[i]) > bmax) bmax = fabsf(v[i]);
+    }
+    const uint8_t sc = orc_e4m3_encode(bmax / 6.0f);
+    ((uint8_t*)sf_row)[b] = sc;  /* little-endian: byte b of the row */
+    const float sd = orc_e4m3_decode(sc);
+    if (sd == 0.0f) continue;
+    const float rs = 1.0f / sd;
+    for (int i = 0; i < 16; ++i) {
+      const uint8_t q = orc_e2m1_encode(v[i] * rs);
+      const int64_t e = b * 16 + i;
+      x_row[e / 2] |= (uint8_t)(e % 2 == 0 ? q : (q << 4));
+    }
+  }
+}
+
+void orc_nvfp4_rows(int64_t T, int64_t K, const uint16_t* hidden, uint8_t* x, int32_t* x_sf,
+                    float* x_scales) {
+  const int64_t Wn = (K / 16 + 3) / 4;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    orc_nvfp4_row(K, hidden + t * K, x + t * (K / 2), x_sf + t * Wn, x_scales + t);
+}
+
 /* S6: dispatch to the batched [E, M_max, .] layout.  Routes are visited in  */
 /* (token, k) order; each takes the next free slot of its expert.  A route   */
 /* whose expert is full is not placed (route_slot = -1) and the function     */
