@@ -70,6 +70,8 @@ def parse():
     ap.add_argument("--config", default="mixtral_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--stage-format", default="fp8", choices=["fp8", "nvfp4"],
+                    help="staging_stress: 1x128 UE8M0 fp8 staging or NVFP4 token staging")
     ap.add_argument("--layout", default="batched", choices=["batched", "contiguous"],
                     help="expert row layout: [E, M_max] slots or expert_offsets")
     return ap.parse_args()
@@ -411,9 +413,17 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
                                                                         device=dev),
                 num_unpadded_tokens=torch.tensor([T], dtype=torch.int32, device=dev))
     s = torch.cuda.current_stream()
+    nvfp4 = args.stage_format == "nvfp4"
+    if nvfp4:
+        x = torch.empty((T, K // 2), dtype=torch.uint8, device=dev)
+        x_sf = torch.empty((T, K // 64), dtype=torch.int32, device=dev)
+        x_scales = torch.empty(T, dtype=torch.float32, device=dev)
 
     def step():
-        B.moe_prepare_inputs(hid, ids, wts, x, x_sf, io, wo, eplb=eplb)
+        if nvfp4:
+            B.moe_prepare_nvfp4_inputs(hid, ids, wts, x, x_sf, x_scales, io, wo, eplb=eplb)
+        else:
+            B.moe_prepare_inputs(hid, ids, wts, x, x_sf, io, wo, eplb=eplb)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -442,25 +452,31 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
     ck = clocks.stop()
     ms = max_over_ranks(world, float(np.mean([a.elapsed_time(b) for a, b in evs])))
     nbytes = staging_bytes(T, K, k, wl)
+    if nvfp4:  # codes K/2 + E4M3 scales K/16 + fp32 scale, instead of K + K/32
+        nbytes += T * (K // 2 + K // 16 + 4) - T * (K + 4 * ((G + 3) // 4))
     gbs = world * nbytes / (ms * 1e-3) / 1e9
     out = dict(metric=METRIC, value=round(gbs, 1), unit="GB/s", n_gpus=world, steps=Ks,
                 warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True,
-                scaling="weak", vs_baseline=None, dtype="bf16->fp8e4m3 (fp32 scale math)",
+                scaling="weak", vs_baseline=None,
+                dtype="bf16->e2m1 (e4m3/16, fp32/token)" if nvfp4 else
+                "bf16->fp8e4m3 (fp32 scale math)",
                 data="synthetic",
-                config=dict(workload="staging_stress", T=T, K=K, top_k=k, experts_logical=c["E"],
+                config=dict(workload="staging_stress", format=args.stage_format, T=T, K=K,
+                            top_k=k, experts_logical=c["E"],
                             experts_physical=wl["num_physical"],
                             l2="inputs larger than L2 and a 512 MB L2 flush before every step"),
                 roofline=dict(bound="hbm", achieved=round(gbs / world, 1), peak=peaks["hbm"],
                               unit="GB/s", frac=round(gbs / world / peaks["hbm"], 4),
-                              traffic=ncu_traffic("staging_stress",
-                                                  "quant_kernel<UE8M0,repack>"),
-                              kernel="quant_kernel<UE8M0,repack>"),
+                              traffic=None if nvfp4 else
+                              ncu_traffic("staging_stress", "quant_kernel<UE8M0,repack>"),
+                              kernel="nvfp4_kernel" if nvfp4 else "quant_kernel<UE8M0,repack>"),
                 e2e=None, gpu_launches=Ks, clocks=ck)
     # end to end: pinned host inputs in, staged outputs back to the host
     hh, ih, wh = (wl["hidden"].pin_memory(), wl["topk_ids"].pin_memory(),
                   wl["topk_weights"].pin_memory())
-    xh = torch.empty((T, K), dtype=torch.uint8).pin_memory()
-    sfh = torch.empty((T, (G + 3) // 4), dtype=torch.int32).pin_memory()
+    xh = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    sfh = torch.empty(x_sf.shape, dtype=x_sf.dtype).pin_memory()
+    xsh = torch.empty(T, dtype=torch.float32).pin_memory() if nvfp4 else None
     ioh = torch.empty((T, k), dtype=torch.int64).pin_memory()
     woh = torch.empty((T, k), dtype=torch.float32).pin_memory()
 
@@ -471,6 +487,8 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
         step()
         xh.copy_(x, non_blocking=True)
         sfh.copy_(x_sf, non_blocking=True)
+        if nvfp4:
+            xsh.copy_(x_scales, non_blocking=True)
         ioh.copy_(io, non_blocking=True)
         woh.copy_(wo, non_blocking=True)
 
@@ -489,15 +507,30 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
     barrier(world)
     e2e_ms = max_over_ranks(world, float(np.mean([a.elapsed_time(b) for a, b in e_ev])))
     h2d = hh.numel() * 2 + ih.numel() * ih.element_size() + wh.numel() * 4
-    d2h = xh.numel() + sfh.numel() * 4 + ioh.numel() * 8 + woh.numel() * 4
+    d2h = xh.numel() + sfh.numel() * 4 + ioh.numel() * 8 + woh.numel() * 4 + \
+        (T * 4 if nvfp4 else 0)
     out["e2e"] = dict(value=round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 1), unit="GB/s",
                       h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
                       ms_per_step=round(e2e_ms, 4))
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
-        secs, thr, n = run_oracle_staging(wl, 2048)
-        out["cpu_baseline"] = dict(value=round(staging_bytes(n, K, k, wl) / secs / 1e9, 4),
-                                   unit="GB/s", cores=thr, kind="oracle",
-                                   sample=f"first {n} tokens of staging_stress, {secs:.1f} s")
+        if nvfp4:
+            import oracle
+            oracle.build()
+            n = 2048
+            bits = wl["hidden"][:n].view(torch.int16).numpy().view(np.uint16)
+            t0 = time.perf_counter()
+            oracle.nvfp4_rows(bits)
+            secs, thr = time.perf_counter() - t0, oracle.num_threads()
+            nb = n * (K * 2 + K // 2 + K // 16 + 4)
+            what = "NVFP4 rows"
+        else:
+            secs, thr, n = run_oracle_staging(wl, 2048)
+            nb = staging_bytes(n, K, k, wl)
+            what = "staging"
+        out["cpu_baseline"] = dict(value=round(nb / secs / 1e9, 4), unit="GB/s", cores=thr,
+                                   kind="oracle",
+                                   sample=f"{what} of the first {n} tokens of staging_stress, "
+                                          f"{secs:.1f} s")
     return out
 
 

@@ -182,6 +182,69 @@ moe_status_t moe_prepare_inputs(const moe_prepare_args_t* args, void* stream);
 size_t moe_prepare_workspace_size(int64_t num_tokens, int64_t top_k, int64_t num_experts);
 
 /* ------------------------------------------------------------------------ */
+/* moe_prepare_nvfp4_inputs                                                  */
+/*                                                                           */
+/* Defined by prepare_megamoe_nvfp4_inputs (kNvfp4DynamicToken) on the page  */
+/* "vllm.model_executor.layers.fused_moe.prepare_megamoe": each token is     */
+/* scaled by its own fp32 x_scales (row amax / 2688) and quantised to E2M1   */
+/* with one E4M3 scale per 16 values.  The kernel body is not on the page;  */
+/* this library computes, in fp32 with IEEE roundings, per token t:          */
+/*   xs = amax / 2688;  v_i = x_i * (1 / xs);                                */
+/*   per 16 values: s = e4m3_rn_satfinite(max|v_i| / 6),                     */
+/*                  q_i = e2m1_rn_satfinite(v_i * (1 / dec(s)));             */
+/* amax == 0 gives xs = 0 and zero codes and scales; a block whose scale    */
+/* rounds to 0 gets zero codes.  x: uint8 [T, K/2], value 2i in the low     */
+/* nibble of byte i; x_sf: int32 [T, K/64], block b's E4M3 byte at byte     */
+/* b % 4 of word b / 4; x_scales: fp32 [T].                                  */
+/* Routing outputs (topk_idx_out, topk_weights_out, EPLB map and load) are  */
+/* exactly those of moe_prepare_inputs.  shared_x (nullable, bf16 [T, K])    */
+/* receives a copy of the hidden rows (the page's BF16 shared input; its     */
+/* MXFP8 shared input is what moe_prepare_inputs writes with shared_x_sf).  */
+/* l2_alpha[e] = w2_global_scale[e] * l2_activation_scale for e <            */
+/* num_local_experts, written even when T == 0 (both NULL or both given).    */
+/* Errors: K % 128 != 0 -> SHAPE; rows of hidden, x, shared_x not 16-byte    */
+/* aligned -> ALIGNMENT; w2_global_scale without l2_alpha -> INVALID.        */
+/* ------------------------------------------------------------------------ */
+typedef struct moe_nvfp4_args {
+  int64_t num_tokens, hidden_size, top_k;
+  const void* hidden; /* bf16 [T, K] */
+  int64_t hidden_stride0;
+  const void* topk_ids;
+  int32_t topk_ids_dtype;
+  int64_t topk_ids_stride0, topk_ids_stride1;
+  const void* topk_weights;
+  int32_t topk_weights_dtype;
+  int64_t topk_weights_stride0, topk_weights_stride1;
+  const uint8_t* is_padding; /* nullable */
+  int64_t is_padding_stride0;
+  uint8_t* x; /* E2M1 pairs [T, K/2] */
+  int64_t x_stride0;
+  int32_t* x_sf; /* packed E4M3 block scales [T, K/64] */
+  int64_t x_sf_stride0;
+  float* x_scales; /* [T] */
+  void* shared_x;  /* nullable bf16 [T, K] copy */
+  int64_t shared_x_stride0;
+  int64_t* topk_idx_out;
+  int64_t topk_idx_out_stride0, topk_idx_out_stride1;
+  float* topk_weights_out;
+  int64_t topk_weights_out_stride0, topk_weights_out_stride1;
+  const int32_t* logical_to_physical; /* EPLB, as in moe_prepare_args_t */
+  int64_t num_logical, map_stride;
+  const int32_t* logical_replica_count;
+  int32_t* expert_load;
+  int64_t num_physical;
+  const uint8_t* should_record;
+  const int32_t* num_unpadded_tokens;
+  const float* w2_global_scale; /* nullable [num_local_experts] */
+  float* l2_alpha;              /* nullable [num_local_experts] */
+  int64_t num_local_experts;
+  float l2_activation_scale;
+  uint32_t* device_status;
+} moe_nvfp4_args_t;
+
+moe_status_t moe_prepare_nvfp4_inputs(const moe_nvfp4_args_t* args, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* moe_prepare_inputs_noalloc                                                */
 /*                                                                           */
 /* No counterpart on the pages: an addition of this library for callers that */

@@ -56,6 +56,31 @@ class PrepareArgs(ctypes.Structure):
     ]
 
 
+class Nvfp4Args(ctypes.Structure):
+    _fields_ = [
+        ("num_tokens", _i64), ("hidden_size", _i64), ("top_k", _i64),
+        ("hidden", _vp), ("hidden_stride0", _i64),
+        ("topk_ids", _vp), ("topk_ids_dtype", _i32),
+        ("topk_ids_stride0", _i64), ("topk_ids_stride1", _i64),
+        ("topk_weights", _vp), ("topk_weights_dtype", _i32),
+        ("topk_weights_stride0", _i64), ("topk_weights_stride1", _i64),
+        ("is_padding", _vp), ("is_padding_stride0", _i64),
+        ("x", _vp), ("x_stride0", _i64),
+        ("x_sf", _vp), ("x_sf_stride0", _i64),
+        ("x_scales", _vp),
+        ("shared_x", _vp), ("shared_x_stride0", _i64),
+        ("topk_idx_out", _vp), ("topk_idx_out_stride0", _i64), ("topk_idx_out_stride1", _i64),
+        ("topk_weights_out", _vp), ("topk_weights_out_stride0", _i64),
+        ("topk_weights_out_stride1", _i64),
+        ("logical_to_physical", _vp), ("num_logical", _i64), ("map_stride", _i64),
+        ("logical_replica_count", _vp), ("expert_load", _vp), ("num_physical", _i64),
+        ("should_record", _vp), ("num_unpadded_tokens", _vp),
+        ("w2_global_scale", _vp), ("l2_alpha", _vp), ("num_local_experts", _i64),
+        ("l2_activation_scale", ctypes.c_float),
+        ("device_status", _vp),
+    ]
+
+
 class ExpertsArgs(ctypes.Structure):
     _fields_ = [
         ("num_experts", _i64), ("max_tokens_per_expert", _i64), ("hidden_size", _i64),
@@ -250,6 +275,55 @@ def moe_prepare_inputs_noalloc(hidden, topk_ids, topk_weights, x, x_sf, topk_idx
     a.device_status = _ptr(device_status)
     _check("moe_prepare_inputs_noalloc",
            load().moe_prepare_inputs_noalloc(ctypes.byref(a), _stream(stream)))
+
+
+def moe_prepare_nvfp4_inputs(hidden, topk_ids, topk_weights, x, x_sf, x_scales, topk_idx_out,
+                             topk_weights_out, is_padding=None, shared_x=None, eplb=None,
+                             w2_global_scale=None, l2_alpha=None, l2_activation_scale=1.0,
+                             device_status=None, stream=None):
+    """NVFP4 token staging (E2M1 + E4M3 per 16 + fp32 per-token scale) and the
+    top-k repack.  x: uint8 [T, K/2]; x_sf: int32 [T, K/64]; x_scales: fp32 [T].
+    See include/moe_prep.h."""
+    T, K = hidden.shape
+    a = Nvfp4Args()
+    a.num_tokens, a.hidden_size = T, K
+    a.top_k = topk_ids.shape[1] if topk_ids.dim() == 2 else 0
+    a.hidden, a.hidden_stride0 = _ptr(hidden), hidden.stride(0)
+    a.topk_ids = _ptr(topk_ids)
+    a.topk_ids_dtype = MOE_IDS_INT64 if topk_ids.dtype == torch.int64 else MOE_IDS_INT32
+    a.topk_ids_stride0, a.topk_ids_stride1 = topk_ids.stride(0), topk_ids.stride(1)
+    a.topk_weights = _ptr(topk_weights)
+    a.topk_weights_dtype = MOE_WEIGHTS_BF16 if topk_weights.dtype == torch.bfloat16 else \
+        MOE_WEIGHTS_FP32
+    a.topk_weights_stride0, a.topk_weights_stride1 = topk_weights.stride(0), topk_weights.stride(1)
+    if is_padding is not None:
+        a.is_padding, a.is_padding_stride0 = _ptr(is_padding), is_padding.stride(0)
+    a.x, a.x_stride0 = _ptr(x), x.stride(0)
+    a.x_sf, a.x_sf_stride0 = _ptr(x_sf), x_sf.stride(0)
+    a.x_scales = _ptr(x_scales)
+    if shared_x is not None:
+        a.shared_x, a.shared_x_stride0 = _ptr(shared_x), shared_x.stride(0)
+    a.topk_idx_out = _ptr(topk_idx_out)
+    a.topk_idx_out_stride0, a.topk_idx_out_stride1 = topk_idx_out.stride(0), topk_idx_out.stride(1)
+    a.topk_weights_out = _ptr(topk_weights_out)
+    a.topk_weights_out_stride0 = topk_weights_out.stride(0)
+    a.topk_weights_out_stride1 = topk_weights_out.stride(1)
+    if eplb:
+        l2p = eplb["logical_to_physical"]
+        a.logical_to_physical, a.num_logical, a.map_stride = _ptr(l2p), l2p.shape[0], l2p.stride(0)
+        a.logical_replica_count = _ptr(eplb["logical_replica_count"])
+        load_t = eplb.get("expert_load")
+        if load_t is not None:
+            a.expert_load, a.num_physical = _ptr(load_t), load_t.numel()
+        a.should_record = _ptr(eplb.get("should_record"))
+        a.num_unpadded_tokens = _ptr(eplb.get("num_unpadded_tokens"))
+    if l2_alpha is not None:
+        a.w2_global_scale, a.l2_alpha = _ptr(w2_global_scale), _ptr(l2_alpha)
+        a.num_local_experts = l2_alpha.numel()
+    a.l2_activation_scale = float(l2_activation_scale)
+    a.device_status = _ptr(device_status)
+    _check("moe_prepare_nvfp4_inputs",
+           load().moe_prepare_nvfp4_inputs(ctypes.byref(a), _stream(stream)))
 
 
 def moe_batched_experts(output, hidden, a_scale, w13, w13_scale, w2, w2_scale,

@@ -52,6 +52,7 @@ int resident_blocks(const void* kernel, int block) {
 
 size_t prepare_workspace_size(int64_t T, int64_t k, int64_t E);
 moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s);
+moe_status_t launch_nvfp4(const moe_nvfp4_args_t* a, cudaStream_t s);
 moe_status_t launch_topk_reduce(const void* expert_out, int64_t E, int64_t M_max, int64_t K,
                                 const int64_t* idx, const int32_t* slot, const float* w,
                                 int64_t T, int64_t top_k, void* out, cudaStream_t s);
@@ -156,6 +157,48 @@ moe_status_t moe_prepare_inputs(const moe_prepare_args_t* a, void* stream) {
     return set_error(MOE_ERR_INVALID_ARGUMENT, "expert_offsets needs the dispatch outputs (x_b)");
   }
   return launch_prepare(a, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_prepare_nvfp4_inputs(const moe_nvfp4_args_t* a, void* stream) {
+  g_last_error[0] = '\0';
+  if (a == nullptr) return set_error(MOE_ERR_INVALID_ARGUMENT, "args is NULL");
+  if (a->num_tokens < 0 || a->hidden_size < 0 || a->top_k < 0 || a->num_local_experts < 0)
+    return set_error(MOE_ERR_INVALID_ARGUMENT, "negative size");
+  if ((a->w2_global_scale == nullptr) != (a->l2_alpha == nullptr))
+    return set_error(MOE_ERR_INVALID_ARGUMENT, "w2_global_scale and l2_alpha go together");
+  if (a->l2_alpha != nullptr && a->num_local_experts == 0)
+    return set_error(MOE_ERR_INVALID_ARGUMENT, "l2_alpha needs num_local_experts > 0");
+  if (a->num_tokens == 0 && a->l2_alpha == nullptr) return MOE_OK;
+  if (a->hidden_size % 128 != 0)
+    return set_error(MOE_ERR_SHAPE, "hidden_size %lld is not a multiple of 128",
+                     (long long)a->hidden_size);
+  if (a->num_tokens > 0) {
+    if (a->top_k < 1) return set_error(MOE_ERR_SHAPE, "top_k must be >= 1");
+    if (a->topk_ids_dtype != MOE_IDS_INT32 && a->topk_ids_dtype != MOE_IDS_INT64)
+      return set_error(MOE_ERR_INVALID_ARGUMENT, "bad topk_ids_dtype");
+    if (a->topk_weights_dtype != MOE_WEIGHTS_FP32 && a->topk_weights_dtype != MOE_WEIGHTS_BF16)
+      return set_error(MOE_ERR_INVALID_ARGUMENT, "bad topk_weights_dtype");
+    if (!a->hidden || !a->x || !a->x_sf || !a->x_scales || !a->topk_ids || !a->topk_weights ||
+        !a->topk_idx_out || !a->topk_weights_out)
+      return set_error(MOE_ERR_INVALID_ARGUMENT, "a required pointer is NULL");
+    const int64_t K = a->hidden_size;
+    if (a->hidden_stride0 < K || a->x_stride0 < K / 2 || a->x_sf_stride0 < K / 64 ||
+        (a->shared_x != nullptr && a->shared_x_stride0 < K))
+      return set_error(MOE_ERR_SHAPE, "row stride smaller than the row");
+    if (!aligned16(a->hidden) || (a->hidden_stride0 * 2) % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(a->x) & 3u) != 0 || a->x_stride0 % 4 != 0 ||
+        (a->shared_x != nullptr &&
+         (!aligned16(a->shared_x) || (a->shared_x_stride0 * 2) % 16 != 0)))
+      return set_error(MOE_ERR_ALIGNMENT, "hidden/shared_x rows must start on 16-byte and x "
+                                          "rows on 4-byte boundaries");
+    if (a->logical_to_physical != nullptr &&
+        (a->logical_replica_count == nullptr || a->num_logical <= 0 || a->map_stride <= 0))
+      return set_error(MOE_ERR_INVALID_ARGUMENT,
+                       "EPLB needs logical_replica_count, num_logical and map_stride");
+    if (a->expert_load != nullptr && a->num_physical <= 0)
+      return set_error(MOE_ERR_INVALID_ARGUMENT, "expert_load needs num_physical > 0");
+  }
+  return launch_nvfp4(a, static_cast<cudaStream_t>(stream));
 }
 
 size_t moe_batched_experts_workspace_size(int64_t num_experts, int64_t max_tokens_per_expert,

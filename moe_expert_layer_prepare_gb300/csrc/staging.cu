@@ -23,6 +23,8 @@
 //                  Without dispatch the repack is folded into this kernel.
 #include <cstdio>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -478,6 +480,164 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// NVFP4 token staging: per-token fp32 scale amax/2688, E2M1 codes with one
+// E4M3 scale per 16 values.  One warp per token, two passes over the row:
+// the first finds the row amax, the second (the row is then in L1/L2)
+// quantises.  Lane l takes the 8-value chunks l, l+32, ...; lanes 2m and
+// 2m+1 hold one 16-value block, lanes 8g..8g+7 one scale word.
+// ---------------------------------------------------------------------------
+struct Nvfp4Params {
+  int64_t T, K;
+  const uint16_t* hidden;
+  int64_t hs0;
+  uint8_t* x;
+  int64_t xs0;
+  uint32_t* x_sf;
+  int64_t sfs0;
+  float* x_scales;
+  uint16_t* shared_x;
+  int64_t shs0;
+  const float* w2gs;
+  float* l2_alpha;
+  int64_t n_local;
+  float l2s;
+};
+
+// Two fp32 -> two E2M1 codes (round to nearest even, saturating to +-6),
+// lo in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 b; cvt.rn.satfinite.e2m1x2.f32 b, %2, %1; cvt.u32.u8 %0, b; }"
+      : "=r"(r)
+      : "f"(lo), "f"(hi));
+  return r;
+}
+
+// E4M3 code -> fp32 (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h2;
+  asm("{ .reg .b16 c; cvt.u16.u32 c, %1; cvt.rn.f16x2.e4m3x2 %0, c; }" : "=r"(h2) : "r"(code));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// Quantise one 8-value chunk c (lanes 2m, 2m+1 form a 16-value block; all
+// 32 lanes call this together).
+__device__ __forceinline__ void nvfp4_chunk(const Nvfp4Params& q, int64_t t, int64_t c, bool act,
+                                            uint4 v, float inv, int lane) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+  float lmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __fmul_rn(bf16_bits_to_f32(u[i] & 0xFFFFu), inv);
+    f[2 * i + 1] = __fmul_rn(bf16_bits_to_f32(u[i] >> 16), inv);
+    lmax = fmaxf(lmax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+  }
+  if (q.shared_x != nullptr && act) st_v4(q.shared_x + t * q.shs0 + c * 8, v);
+  const float bmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, 1));
+  const uint32_t sc = e4m3x2(__fdiv_rn(bmax, 6.0f), 0.0f) & 0xFFu;
+  const float sd = e4m3_to_f32(sc);
+  uint32_t codes = 0;  // a block whose scale is 0 keeps zero codes (no -0)
+  if (sd > 0.0f) {
+    const float rs = __frcp_rn(sd);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      codes |= e2m1x2(__fmul_rn(f[2 * i], rs), __fmul_rn(f[2 * i + 1], rs)) << (8 * i);
+  }
+  if (act) reinterpret_cast<uint32_t*>(q.x + t * q.xs0)[c] = codes;
+  // scale word of lanes 8g..8g+7: the blocks of lanes 8g, 8g+2, 8g+4, 8g+6
+  const int g0 = lane & ~7;
+  const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, sc, g0);
+  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sc, g0 + 2);
+  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sc, g0 + 4);
+  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sc, g0 + 6);
+  if (act && (lane & 7) == 0) q.x_sf[t * q.sfs0 + c / 8] = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
+__device__ __forceinline__ float bf16x8_absmax(uint4 v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(u[i] & 0xFFFFu)), fabsf(bf16_bits_to_f32(u[i] >> 16))));
+  return m;
+}
+
+// REG: rows of at most 8192 values are held in registers (up to 32 16-byte
+// chunks per lane, all loads in flight at once); longer rows are read twice,
+// the second time from L1/L2.
+template <typename IdT, typename WT, bool REG>
+__global__ void __launch_bounds__(256) nvfp4_kernel(Nvfp4Params q, StageParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (blockIdx.x == 0 && q.l2_alpha != nullptr)
+    for (int64_t e = threadIdx.x; e < q.n_local; e += blockDim.x)
+      q.l2_alpha[e] = __fmul_rn(q.w2gs[e], q.l2s);
+  const int64_t chunks = q.K / 8;  // a multiple of 16 (K % 128 == 0)
+  for (int64_t t = gwarp; t < q.T; t += nwarps) {
+    const uint16_t* row = q.hidden + t * q.hs0;
+    float amax = 0.0f;
+    if constexpr (REG) {
+      uint4 v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int64_t c = lane + 32 * i;
+        v[i] = c < chunks ? ld_stream_v4(row + c * 8) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, bf16x8_absmax(v[i]));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      const float xs = __fdiv_rn(amax, 2688.0f);
+      if (lane == 0) q.x_scales[t] = xs;
+      const float inv = amax > 0.0f ? __frcp_rn(xs) : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (32 * i < chunks)  // warp-uniform
+          nvfp4_chunk(q, t, lane + 32 * i, lane + 32 * i < chunks, v[i], inv, lane);
+      }
+    } else {
+      for (int64_t c = lane; c < chunks; c += 32) amax = fmaxf(amax, bf16x8_absmax(ld_stream_v4(row + c * 8)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      const float xs = __fdiv_rn(amax, 2688.0f);
+      if (lane == 0) q.x_scales[t] = xs;
+      const float inv = amax > 0.0f ? __frcp_rn(xs) : 0.0f;
+      for (int64_t c0 = 0; c0 < chunks; c0 += 32) {
+        const int64_t c = c0 + lane;
+        const bool act = c < chunks;
+        const uint4 v = act ? ld_stream_v4(row + c * 8) : make_uint4(0, 0, 0, 0);
+        nvfp4_chunk(q, t, c, act, v, inv, lane);
+      }
+    }
+  }
+  // routing: the same repack as the fp8 staging
+  bool record_on;
+  int64_t unpadded;
+  record_flags(p, record_on, unpadded);
+  const int64_t R = p.T * p.top_k;
+  if (record_on && p.load != nullptr && p.num_physical <= kLoadBins) {
+    __shared__ int s_load[kLoadBins];
+    const int64_t nrep = min((int64_t)gridDim.x, (int64_t)kLoadBlocks);
+    if (blockIdx.x < nrep) {
+      const int64_t per = (R + nrep - 1) / nrep;
+      repack_recorded<IdT, WT>(p, blockIdx.x * per, min(R, (blockIdx.x + 1) * per), unpadded,
+                               s_load);
+    }
+  } else {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R;
+         r += (int64_t)gridDim.x * blockDim.x)
+      repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
+  }
+}
+
 }  // namespace moe
 
 // ---------------------------------------------------------------------------
@@ -627,6 +787,72 @@ moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s) {
                  : launch_typed<int64_t, float>(p, dispatch, a->sf_mode, s);
   return wbf16 ? launch_typed<int32_t, uint16_t>(p, dispatch, a->sf_mode, s)
                : launch_typed<int32_t, float>(p, dispatch, a->sf_mode, s);
+}
+
+
+template <typename IdT, typename WT>
+static moe_status_t launch_nvfp4_typed(const moe::Nvfp4Params& q, const StageParams& p,
+                                       cudaStream_t s) {
+  auto k = q.K <= 8192 ? moe::nvfp4_kernel<IdT, WT, true> : moe::nvfp4_kernel<IdT, WT, false>;
+  int64_t blocks = (q.T + 7) / 8;
+  if (blocks < 1) blocks = 1;
+  const int64_t cap = (int64_t)num_sms() * resident_blocks(reinterpret_cast<const void*>(k), 256);
+  if (blocks > cap) blocks = cap;
+  cudaError_t e = launch_pdl(k, dim3((unsigned)blocks), dim3(256), 0, s, q, p);
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "nvfp4 launch: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+moe_status_t launch_nvfp4(const moe_nvfp4_args_t* a, cudaStream_t s) {
+  moe::Nvfp4Params q{};
+  q.T = a->num_tokens;
+  q.K = a->hidden_size;
+  q.hidden = static_cast<const uint16_t*>(a->hidden);
+  q.hs0 = a->hidden_stride0;
+  q.x = a->x;
+  q.xs0 = a->x_stride0;
+  q.x_sf = reinterpret_cast<uint32_t*>(a->x_sf);
+  q.sfs0 = a->x_sf_stride0;
+  q.x_scales = a->x_scales;
+  q.shared_x = static_cast<uint16_t*>(a->shared_x);
+  q.shs0 = a->shared_x_stride0;
+  q.w2gs = a->w2_global_scale;
+  q.l2_alpha = a->l2_alpha;
+  q.n_local = a->num_local_experts;
+  q.l2s = a->l2_activation_scale;
+  StageParams p{};
+  p.T = a->num_tokens;
+  p.K = a->hidden_size;
+  p.top_k = a->top_k;
+  p.ids = a->topk_ids;
+  p.is0 = a->topk_ids_stride0;
+  p.is1 = a->topk_ids_stride1;
+  p.wts = a->topk_weights;
+  p.ws0 = a->topk_weights_stride0;
+  p.ws1 = a->topk_weights_stride1;
+  p.pad = a->is_padding;
+  p.ps0 = a->is_padding_stride0;
+  p.ids_out = a->topk_idx_out;
+  p.ios0 = a->topk_idx_out_stride0;
+  p.ios1 = a->topk_idx_out_stride1;
+  p.w_out = a->topk_weights_out;
+  p.wos0 = a->topk_weights_out_stride0;
+  p.wos1 = a->topk_weights_out_stride1;
+  p.l2p = a->logical_to_physical;
+  p.num_logical = a->num_logical;
+  p.map_stride = a->map_stride;
+  p.rep_count = a->logical_replica_count;
+  p.load = a->expert_load;
+  p.num_physical = a->num_physical;
+  p.record = a->should_record;
+  p.num_unpadded = a->num_unpadded_tokens;
+  p.status = a->device_status;
+  const bool i64 = a->topk_ids_dtype == MOE_IDS_INT64;
+  const bool bf = a->topk_weights_dtype == MOE_WEIGHTS_BF16;
+  if (i64) return bf ? launch_nvfp4_typed<int64_t, uint16_t>(q, p, s)
+                     : launch_nvfp4_typed<int64_t, float>(q, p, s);
+  return bf ? launch_nvfp4_typed<int32_t, uint16_t>(q, p, s)
+            : launch_nvfp4_typed<int32_t, float>(q, p, s);
 }
 
 }  // namespace moe_host

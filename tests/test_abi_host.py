@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     for must in ["moe_prepare_inputs", "moe_batched_experts", "moe_topk_reduce",
                  "moe_abi_version", "moe_last_error", "moe_prepare_workspace_size",
-                 "moe_batched_experts_workspace_size"]:
+                 "moe_batched_experts_workspace_size", "moe_prepare_nvfp4_inputs"]:
         assert must in names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/moe_prep.h but not exported"
@@ -150,3 +150,28 @@ def test_workspace_sizes(lib):
     assert s13 >= 256 * 1024 * 2048 + 256 * 1024 * 4 * 4
     s2 = lib.moe_batched_experts_workspace_size(8, 64, 4096, 14336, 128, 2)
     assert s2 > 0
+
+
+def test_nvfp4_rejects(lib):
+    def args(**kw):
+        a = B.Nvfp4Args()
+        a.num_tokens, a.hidden_size, a.top_k = 8, 256, 2
+        a.hidden, a.hidden_stride0 = FAKE, 256
+        a.topk_ids, a.topk_ids_stride0, a.topk_ids_stride1 = FAKE, 2, 1
+        a.topk_weights, a.topk_weights_stride0, a.topk_weights_stride1 = FAKE, 2, 1
+        a.x, a.x_stride0, a.x_sf, a.x_sf_stride0, a.x_scales = FAKE, 128, FAKE, 4, FAKE
+        a.topk_idx_out, a.topk_idx_out_stride0, a.topk_idx_out_stride1 = FAKE, 2, 1
+        a.topk_weights_out, a.topk_weights_out_stride0, a.topk_weights_out_stride1 = FAKE, 2, 1
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    run = lambda a: lib.moe_prepare_nvfp4_inputs(ctypes.byref(a), None)  # noqa: E731
+    assert run(args(hidden_size=192, hidden_stride0=192, x_stride0=96, x_sf_stride0=3)) == 2
+    assert run(args(x_scales=None)) == 1
+    assert run(args(w2_global_scale=FAKE)) == 1            # without l2_alpha
+    assert run(args(l2_alpha=FAKE, w2_global_scale=FAKE)) == 1  # no local experts
+    assert run(args(hidden=FAKE + 8)) == 4
+    assert run(args(x=FAKE + 2)) == 4
+    assert run(args(x_sf_stride0=3)) == 2                  # K/64 = 4 words per row
+    assert run(args(top_k=0)) == 2
+    assert run(args(num_tokens=0)) == 0                    # nothing to do
