@@ -121,7 +121,8 @@ typedef enum moe_activation { MOE_ACT_SILU = 0 } moe_activation_t;
 /* Errors: T == 0 -> MOE_OK, nothing enqueued.  K % 128 != 0 -> SHAPE.       */
 /* x_sf given iff sf_mode != NONE, else INVALID_ARGUMENT.  top_k < 1 ->       */
 /* SHAPE.  hidden / x rows must start on 16-byte boundaries (ALIGNMENT).     */
-/* Dispatch needs workspace of moe_prepare_workspace_size() bytes (WORKSPACE).*/
+/* Dispatch needs workspace of moe_prepare_workspace_size() bytes (WORKSPACE)*/
+/* and top_k <= 32 (UNSUPPORTED).                                            */
 /* ------------------------------------------------------------------------ */
 typedef struct moe_prepare_args {
   int64_t num_tokens;  /* T >= 0 */

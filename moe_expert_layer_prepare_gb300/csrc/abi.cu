@@ -136,6 +136,8 @@ moe_status_t moe_prepare_inputs(const moe_prepare_args_t* a, void* stream) {
   if (a->x_b != nullptr) {
     if (a->sf_mode == MOE_SF_NONE)
       return set_error(MOE_ERR_UNSUPPORTED, "dispatch requires quantised (UE8M0 or fp32) scales");
+    if (a->top_k > 32)
+      return set_error(MOE_ERR_UNSUPPORTED, "dispatch supports top_k <= 32");
     if (a->num_experts <= 0 || a->num_experts > 1024 || a->max_tokens_per_expert <= 0)
       return set_error(MOE_ERR_SHAPE, "dispatch needs 0 < num_experts <= 1024, M_max > 0");
     if (!a->sf_b || !a->expert_num_tokens || !a->route_slot)

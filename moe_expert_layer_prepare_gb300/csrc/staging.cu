@@ -330,23 +330,29 @@ __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int6
 
     if constexpr (DISPATCH) {
       const int64_t K = p.K;
-      for (int64_t j = 0; j < p.top_k; ++j) {
-        const int64_t r = t * p.top_k + j;
-        const int64_t e = p.ids_out[t * p.ios0 + j * p.ios1];
-        int64_t slot = -1, row = -1;
+      // Lane j works out route j's destination row (three dependent loads),
+      // so the top_k chains run side by side; the rows are then broadcast.
+      int64_t my_slot = -1, my_row = -1;
+      if (lane < p.top_k) {
+        const int64_t r = t * p.top_k + lane;
+        const int64_t e = p.ids_out[t * p.ios0 + lane * p.ios1];
         if (e >= 0 && e < p.E) {
           // contiguous layout: the scanned offsets already include the
           // expert's first row, so the slot is the row
-          slot = (int64_t)__ldcg(&p.hist[(r >> 10) * p.E + e]) + p.local_rank[r];
+          my_slot = (int64_t)__ldcg(&p.hist[(r >> 10) * p.E + e]) + p.local_rank[r];
           if (p.offsets != nullptr) {
-            row = slot;
-          } else if (slot < p.M_max) {
-            row = e * p.M_max + slot;
+            my_row = my_slot;
+          } else if (my_slot < p.M_max) {
+            my_row = e * p.M_max + my_slot;
           } else {
-            slot = -1;
+            my_slot = -1;
           }
         }
-        if (slot >= 0) {
+        if (w == 0) p.route_slot[r] = (int32_t)my_slot;
+      }
+      for (int64_t j = 0; j < p.top_k; ++j) {
+        const int64_t row = __shfl_sync(0xFFFFFFFFu, my_row, (int)j);
+        if (row >= 0) {
           uint8_t* brow = p.x_b + row * K;
           if (actA) st_v2(brow + offA, qA);
           if (actB) st_v2(brow + offB, qB);
@@ -360,7 +366,6 @@ __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int6
             }
           }
         }
-        if (w == 0 && lane == 0) p.route_slot[r] = (int32_t)slot;
       }
     }
   }
