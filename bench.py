@@ -42,11 +42,12 @@ FLUSH_BYTES = 512 << 20  # > 129 MB L2
 GEMM_SRC = "moe_expert_layer_prepare_gb300/csrc/experts_gemm.cu"
 STAGING_SRC = "moe_expert_layer_prepare_gb300/csrc/staging.cu"
 NCU_TRAFFIC = {
-    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (952.71e6, GEMM_SRC, "511edd3914739514"),
-    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1148.09e6, GEMM_SRC,
-                                                       "511edd3914739514"),
-    ("staging_stress", "quant_kernel<UE8M0,repack>"): (296.73e6, STAGING_SRC,
-                                                       "65cdc72dce59110e"),
+    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (949.52e6, GEMM_SRC, "02ba55e071648898"),
+    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1144.66e6, GEMM_SRC,
+                                                       "02ba55e071648898"),
+    ("staging_stress", "quant_kernel<UE8M0,repack>"): (296.94e6, STAGING_SRC,
+                                                       "867331b02a770e7d"),
+    ("staging_stress", "nvfp4_kernel"): (248.88e6, STAGING_SRC, "867331b02a770e7d"),
 }
 
 
@@ -467,8 +468,8 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
                             l2="inputs larger than L2 and a 512 MB L2 flush before every step"),
                 roofline=dict(bound="hbm", achieved=round(gbs / world, 1), peak=peaks["hbm"],
                               unit="GB/s", frac=round(gbs / world / peaks["hbm"], 4),
-                              traffic=None if nvfp4 else
-                              ncu_traffic("staging_stress", "quant_kernel<UE8M0,repack>"),
+                              traffic=ncu_traffic("staging_stress", "nvfp4_kernel" if nvfp4
+                                                  else "quant_kernel<UE8M0,repack>"),
                               kernel="nvfp4_kernel" if nvfp4 else "quant_kernel<UE8M0,repack>"),
                 e2e=None, gpu_launches=Ks, clocks=ck)
     # end to end: pinned host inputs in, staged outputs back to the host
