@@ -167,7 +167,13 @@ def build_workload(name, device):
 
 
 def algorithmic(wl):
-    """Valid-row FLOPs and algorithmic bytes per kernel."""
+    """Valid-row FLOPs and algorithmic bytes per kernel.
+
+    FLOPs count routed rows only (6*N*K per route: 4*N*K in w13, 2*N*K in w2).
+    Bytes count each kernel's compulsory traffic: the weights and block scales
+    of the experts with at least one route, the routed activation rows and
+    scales read, and the outputs written.
+    """
     c = wl["cfg"]
     T, K, N, E, k = c["T"], c["K"], c["N"], c["E"], c["top_k"]
     ids = wl["topk_ids"].cpu().numpy()
