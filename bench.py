@@ -84,7 +84,8 @@ def dist_setup(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
     return world, rank, local
 
@@ -99,7 +100,8 @@ def max_over_ranks(world, v):
     if world <= 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
