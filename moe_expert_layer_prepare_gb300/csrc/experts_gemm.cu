@@ -277,6 +277,12 @@ struct Unit {
   int gmt;   // global m-tile index (split-K counters of the contiguous layout)
 };
 
+// Units are numbered expert by expert.  Inside an expert, w2 takes them
+// m-tile-major (tile (mt, nt) at mt * n_tiles + nt) and w13 n-tile-major, so
+// that the m-tiles sharing one w13 weight tile run side by side and the
+// second and third reads of it hit L2 (measured: prefill w13 -2%, w2 +3% with
+// the same order, so w2 keeps the other one).
+template <bool W13>
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const int* prefix, int u,
                                             const int* cnt) {
   Unit w;
@@ -291,10 +297,19 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const int* pref
     if (prefix[mid] <= mt_idx) lo = mid; else hi = mid - 1;
   }
   w.e = lo;
-  w.mt = mt_idx - prefix[lo];
+  if constexpr (W13) {
+    const int mt_e = prefix[lo + 1] - prefix[lo];
+    const int l = u - prefix[lo] * per_mt;
+    w.nt = l / (mt_e * p.splits);
+    const int r2 = l - w.nt * (mt_e * p.splits);
+    w.mt = r2 / p.splits;
+    w.ks = r2 - w.mt * p.splits;
+  } else {
+    w.mt = mt_idx - prefix[lo];
+  }
   w.rows = min(BM, cnt[lo] - w.mt * BM);
   w.row0 = (p.offsets != nullptr ? __ldg(p.offsets + lo) : lo * p.M_max) + w.mt * BM;
-  w.gmt = mt_idx;
+  w.gmt = prefix[lo] + w.mt;
   const int per = (p.KB + p.splits - 1) / p.splits;
   w.kb0 = w.ks * per;
   w.kb1 = min(p.KB, w.kb0 + per);
@@ -415,7 +430,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued_mask = 0, issued_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit w = decode_unit(p, prefix, u, cnt);
+        const Unit w = decode_unit<W13>(p, prefix, u, cnt);
         const int a_row0 = w.row0;
         const int n_boxes = (w.rows + A_BOX_ROWS - 1) / A_BOX_ROWS;
         const uint32_t tx = (uint32_t)(n_boxes * A_BOX_ROWS * BK + B_BYTES);
@@ -469,7 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       bool any = false;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit w = decode_unit(p, prefix, u, cnt);
+        const Unit w = decode_unit<W13>(p, prefix, u, cnt);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           const bool ready = mbar_wait(tempty0 + 8 * ab, aphase ^ 1u, abort_flag, p.status) &&
                              mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status);
@@ -537,7 +552,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       cg[c] = W13 ? (uint32_t)((c < 2 ? 0 : 128) + h * 64 + (c & 1) * 32)
                   : (uint32_t)(h * 128 + c * 32);
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const Unit w = decode_unit(p, prefix, u, cnt);
+      const Unit w = decode_unit<W13>(p, prefix, u, cnt);
       const bool row_ok = row_local < w.rows;
       const bool warp_active = q * 32 < w.rows;   // warp-uniform
       const int64_t grow = (int64_t)w.row0 + row_local;
