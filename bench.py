@@ -42,9 +42,9 @@ FLUSH_BYTES = 512 << 20  # > 129 MB L2
 GEMM_SRC = "moe_expert_layer_prepare_gb300/csrc/experts_gemm.cu"
 STAGING_SRC = "moe_expert_layer_prepare_gb300/csrc/staging.cu"
 NCU_TRAFFIC = {
-    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (949.68e6, GEMM_SRC, "aa7ec99e1cf9c6ab"),
-    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1144.04e6, GEMM_SRC,
-                                                       "aa7ec99e1cf9c6ab"),
+    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (952.31e6, GEMM_SRC, "27b77fc5e84f75d5"),
+    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1040.37e6, GEMM_SRC,
+                                                       "27b77fc5e84f75d5"),
     ("staging_stress", "quant_kernel<UE8M0,repack>"): (296.94e6, STAGING_SRC,
                                                        "867331b02a770e7d"),
     ("staging_stress", "nvfp4_kernel"): (248.88e6, STAGING_SRC, "867331b02a770e7d"),
