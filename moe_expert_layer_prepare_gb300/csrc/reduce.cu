@@ -6,9 +6,10 @@
 // ("vllm.model_executor.layers.fused_moe.experts.fused_humming_moe").
 //
 // One warp per (token, 256-column chunk); each lane owns 8 columns (16 bytes).
-// For each j in ascending order the routed expert row is read with a
-// streaming 16-byte load, weighted in fp32 and accumulated; one bf16 rounding
-// at the end.  HBM-bound: each routed row is read once, each output row
+// The routes' rows and weights are resolved once per warp (one lane per
+// route) and the routed expert rows are read eight at a time with streaming
+// 16-byte loads, then weighted in fp32 and accumulated in ascending j; one
+// bf16 rounding at the end.  HBM-bound: each routed row is read once, each output row
 // written once.
 #include "common.cuh"
 
@@ -23,6 +24,19 @@ struct ReduceParams {
   int64_t T, top_k;
   uint16_t* out;         // bf16 [T, K]
 };
+
+// Row of route j of token t in expert_out, or -1 when the route is unrouted
+// or out of range; its weight goes to *w.
+__device__ __forceinline__ int64_t route_row(const ReduceParams& p, int64_t t, int64_t j,
+                                             float* w) {
+  const int32_t s = p.slot[t * p.top_k + j];
+  *w = p.w[t * p.top_k + j];
+  if (p.idx != nullptr) {  // batched: (expert, slot)
+    const int64_t e = p.idx[t * p.top_k + j];
+    return (e >= 0 && s >= 0 && e < p.E && s < p.M_max) ? e * p.M_max + s : -1;
+  }
+  return (s >= 0 && s < p.E * p.M_max) ? (int64_t)s : -1;  // contiguous: the slot is the row
+}
 
 __global__ void __launch_bounds__(256) topk_reduce_kernel(ReduceParams p) {
   const int lane = threadIdx.x & 31;
@@ -41,25 +55,39 @@ __global__ void __launch_bounds__(256) topk_reduce_kernel(ReduceParams p) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int64_t j = 0; j < p.top_k; ++j) {
-      const int32_t s = p.slot[t * p.top_k + j];
-      int64_t row;
-      if (p.idx != nullptr) {  // batched: (expert, slot)
-        const int64_t e = p.idx[t * p.top_k + j];
-        if (e < 0 || s < 0 || e >= p.E || s >= p.M_max) continue;
-        row = e * p.M_max + s;
-      } else {  // contiguous: the slot is the row
-        if (s < 0 || s >= p.E * p.M_max) continue;
-        row = s;
-      }
-      const float wt = p.w[t * p.top_k + j];
-      if (active) {
-        const uint4 v = ld_stream_v4(p.expert_out + row * p.K + c0);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    // Lane j < min(top_k, 32) resolves route j's row and weight once; the
+    // rows are then read in groups of 8 with all loads in flight before the
+    // sums, which stay in ascending j.  Routes past 32 resolve directly.
+    int64_t my_row = -1;
+    float my_w = 0.0f;
+    if (lane < p.top_k) my_row = route_row(p, t, lane, &my_w);
+    for (int64_t j0 = 0; j0 < p.top_k; j0 += 8) {
+      uint4 v[8];
+      float wt[8];
+      bool use[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[2 * i] = fmaf(wt, bf16_bits_to_f32(u[i] & 0xFFFFu), acc[2 * i]);
-          acc[2 * i + 1] = fmaf(wt, bf16_bits_to_f32(u[i] >> 16), acc[2 * i + 1]);
+      for (int i = 0; i < 8; ++i) {
+        const int64_t j = j0 + i;  // warp-uniform
+        int64_t row = -1;
+        wt[i] = 0.0f;
+        if (j < 32) {
+          row = __shfl_sync(0xFFFFFFFFu, my_row, (int)j);
+          wt[i] = __shfl_sync(0xFFFFFFFFu, my_w, (int)j);
+        } else if (j < p.top_k) {
+          row = route_row(p, t, j, &wt[i]);
+        }
+        use[i] = j < p.top_k && row >= 0;
+        v[i] = (use[i] && active) ? ld_stream_v4(p.expert_out + row * p.K + c0)
+                                  : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (!use[i]) continue;
+        const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = fmaf(wt[i], bf16_bits_to_f32(u[q] & 0xFFFFu), acc[2 * q]);
+          acc[2 * q + 1] = fmaf(wt[i], bf16_bits_to_f32(u[q] >> 16), acc[2 * q + 1]);
         }
       }
     }

@@ -18,20 +18,35 @@ def cuda():
     return torch.device("cuda")
 
 
-@pytest.mark.parametrize("T,k,E,M,K", [(5, 1, 2, 4, 8), (77, 8, 16, 64, 7168),
-                                       (300, 2, 8, 128, 4104)])
-def test_reduce_vs_oracle(cuda, orc, T, k, E, M, K):
+# k = 9 and 40 cross the groups of 8 routes read together and, for 40, the 32
+# routes resolved one per lane; contig passes topk_idx NULL (slot = row).
+@pytest.mark.parametrize("T,k,E,M,K,contig", [(5, 1, 2, 4, 8, False),
+                                              (77, 8, 16, 64, 7168, False),
+                                              (300, 2, 8, 128, 4104, False),
+                                              (61, 9, 4, 32, 520, False),
+                                              (19, 40, 8, 16, 264, False),
+                                              (45, 40, 8, 16, 1032, True),
+                                              (90, 8, 4, 64, 2048, True)])
+def test_reduce_vs_oracle(cuda, orc, T, k, E, M, K, contig):
     rng = np.random.default_rng(T + K)
     out_b = torch.from_numpy(rng.standard_normal((E, M, K), dtype=np.float32)).to(torch.bfloat16)
-    ids = rng.integers(-1, E, size=(T, k)).astype(np.int64)
-    slots = rng.integers(-1, M, size=(T, k)).astype(np.int32)
+    if contig:
+        # rows of the flat [E*M, K] buffer; -1 marks an unrouted slot
+        slots = rng.integers(-1, E * M, size=(T, k)).astype(np.int32)
+        ids = np.where(slots >= 0, 0, -1).astype(np.int64)  # for the bound below
+        rows_all = np.maximum(slots, 0).astype(np.int64)
+    else:
+        ids = rng.integers(-1, E, size=(T, k)).astype(np.int64)
+        slots = rng.integers(-1, M, size=(T, k)).astype(np.int32)
+        rows_all = np.maximum(ids, 0) * M + np.maximum(slots, 0)
     w = rng.random((T, k)).astype(np.float32)
     dev = torch.device("cuda")
     out = torch.full((T, K), 3.0, dtype=torch.bfloat16, device=dev)
-    B.moe_topk_reduce(out_b.to(dev), torch.from_numpy(ids).to(dev),
+    B.moe_topk_reduce(out_b.to(dev), None if contig else torch.from_numpy(ids).to(dev),
                       torch.from_numpy(slots).to(dev), torch.from_numpy(w).to(dev), out)
     torch.cuda.synchronize()
-    ref = orc.topk_reduce(bf16_bits(out_b).reshape(E * M, K), ids, slots, w, M)
+    ref = orc.topk_reduce(bf16_bits(out_b).reshape(E * M, K), None if contig else ids, slots,
+                          w, M)
     got = bf16_vals(bf16_bits(out)).astype(np.float64)
     rv = bf16_vals(ref).astype(np.float64)
     # fp32 sum vs the oracle's fp64 sum: one bf16 rounding of the result plus
@@ -41,7 +56,7 @@ def test_reduce_vs_oracle(cuda, orc, T, k, E, M, K):
     mag = np.zeros((T, K))
     for j in range(k):
         ok = (ids[:, j] >= 0) & (slots[:, j] >= 0)
-        rows = np.where(ok, ids[:, j] * M + slots[:, j], 0)
+        rows = np.where(ok, rows_all[:, j], 0)
         mag += np.where(ok[:, None], np.abs(w[:, j:j + 1]) * np.abs(ob[rows]), 0.0)
     bound = np.abs(rv) * 2.0 ** -7 + mag * k * 2.0 ** -23
     assert np.all(np.abs(got - rv) <= bound)
