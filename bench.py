@@ -45,9 +45,9 @@ NCU_TRAFFIC = {
     ("mixtral_decode", "grouped_gemm_kernel<W13>"): (952.31e6, GEMM_SRC, "27b77fc5e84f75d5"),
     ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1040.37e6, GEMM_SRC,
                                                        "27b77fc5e84f75d5"),
-    ("staging_stress", "quant_kernel<UE8M0,repack>"): (296.94e6, STAGING_SRC,
-                                                       "867331b02a770e7d"),
-    ("staging_stress", "nvfp4_kernel"): (248.88e6, STAGING_SRC, "867331b02a770e7d"),
+    ("staging_stress", "quant_kernel<UE8M0,repack>"): (296.92e6, STAGING_SRC,
+                                                       "e7defe6027b3c631"),
+    ("staging_stress", "nvfp4_kernel"): (248.82e6, STAGING_SRC, "e7defe6027b3c631"),
 }
 
 

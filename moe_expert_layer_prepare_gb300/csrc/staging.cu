@@ -488,10 +488,12 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
 
 // ---------------------------------------------------------------------------
 // NVFP4 token staging: per-token fp32 scale amax/2688, E2M1 codes with one
-// E4M3 scale per 16 values.  One warp per token, two passes over the row:
-// the first finds the row amax, the second (the row is then in L1/L2)
-// quantises.  Lane l takes the 8-value chunks l, l+32, ...; lanes 2m and
-// 2m+1 hold one 16-value block, lanes 8g..8g+7 one scale word.
+// E4M3 scale per 16 values.  One warp per token; lane l owns the 16-value
+// blocks l, l+32, ... (two 16-byte loads each), so a block's scale, its
+// reciprocal and its codes stay in one lane with no shuffles.  Rows of up to
+// 32*NBL blocks are held in registers between the amax pass and the
+// quantisation pass; longer rows (NBL = 0) are read twice, the second time
+// from L2.
 // ---------------------------------------------------------------------------
 struct Nvfp4Params {
   int64_t T, K;
@@ -510,16 +512,6 @@ struct Nvfp4Params {
   float l2s;
 };
 
-// Two fp32 -> two E2M1 codes (round to nearest even, saturating to +-6),
-// lo in the low nibble.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-  uint32_t r;
-  asm("{ .reg .b8 b; cvt.rn.satfinite.e2m1x2.f32 b, %2, %1; cvt.u32.u8 %0, b; }"
-      : "=r"(r)
-      : "f"(lo), "f"(hi));
-  return r;
-}
-
 // E4M3 code -> fp32 (exact).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   uint32_t h2;
@@ -527,99 +519,145 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
-// Quantise one 8-value chunk c (lanes 2m, 2m+1 form a 16-value block; all
-// 32 lanes call this together).
-__device__ __forceinline__ void nvfp4_chunk(const Nvfp4Params& q, int64_t t, int64_t c, bool act,
-                                            uint4 v, float inv, int lane) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-  float f[8];
-  float lmax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __fmul_rn(bf16_bits_to_f32(u[i] & 0xFFFFu), inv);
-    f[2 * i + 1] = __fmul_rn(bf16_bits_to_f32(u[i] >> 16), inv);
-    lmax = fmaxf(lmax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
-  }
-  if (q.shared_x != nullptr && act) st_v4(q.shared_x + t * q.shs0 + c * 8, v);
-  const float bmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, 1));
-  const uint32_t sc = e4m3x2(__fdiv_rn(bmax, 6.0f), 0.0f) & 0xFFu;
-  const float sd = e4m3_to_f32(sc);
-  uint32_t codes = 0;  // a block whose scale is 0 keeps zero codes (no -0)
-  if (sd > 0.0f) {
-    const float rs = __frcp_rn(sd);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      codes |= e2m1x2(__fmul_rn(f[2 * i], rs), __fmul_rn(f[2 * i + 1], rs)) << (8 * i);
-  }
-  if (act) reinterpret_cast<uint32_t*>(q.x + t * q.xs0)[c] = codes;
-  // scale word of lanes 8g..8g+7: the blocks of lanes 8g, 8g+2, 8g+4, 8g+6
-  const int g0 = lane & ~7;
-  const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, sc, g0);
-  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sc, g0 + 2);
-  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sc, g0 + 4);
-  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sc, g0 + 6);
-  if (act && (lane & 7) == 0) q.x_sf[t * q.sfs0 + c / 8] = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+// Eight fp32 -> eight E2M1 codes (round to nearest even, saturating to +-6),
+// value 2i in the low nibble of byte i.
+__device__ __forceinline__ uint32_t e2m1x8(const float* f) {
+  uint32_t r;
+  asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3}; }"
+      : "=r"(r)
+      : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]),
+        "f"(f[7]));
+  return r;
 }
 
-__device__ __forceinline__ float bf16x8_absmax(uint4 v) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(u[i] & 0xFFFFu)), fabsf(bf16_bits_to_f32(u[i] >> 16))));
-  return m;
+// Packed bf16x2 whose halves have magnitudes max(|a|, |b|) (the signs are
+// the xor of the inputs' and are ignored; a NaN half yields the other one).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// REG: rows of at most 8192 values are held in registers (up to 32 16-byte
-// chunks per lane, all loads in flight at once); longer rows are read twice,
-// the second time from L1/L2.
-template <typename IdT, typename WT, bool REG>
-__global__ void __launch_bounds__(256) nvfp4_kernel(Nvfp4Params q, StageParams p) {
+// Magnitude max over the 16 bf16 values of one block, as packed bf16x2.
+__device__ __forceinline__ uint32_t block_absmax2(uint4 a, uint4 b) {
+  return absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(a.x, a.y), absmax_bf16x2(a.z, a.w)),
+                       absmax_bf16x2(absmax_bf16x2(b.x, b.y), absmax_bf16x2(b.z, b.w)));
+}
+
+__device__ __forceinline__ float absmax2_to_f32(uint32_t m) {
+  return fmaxf(__uint_as_float((m & 0x7FFFu) << 16), __uint_as_float(m & 0x7FFF0000u));
+}
+
+// q = x / 6 without the divide's slow path: q0 = x * RN(1/6), the exact
+// remainder r = x - 6 q0 by FMA, then one correction q0 + r * RN(1/6)
+// (Markstein's correction step).  Over all 2^32 fp32 inputs this equals the
+// IEEE quotient except where both are below 2^-126, where E4M3 encodes
+// either one as 0.
+__device__ __forceinline__ float div6(float x) {
+  const float zh = 0.16666667163372039794921875f;  // RN(1/6)
+  const float q0 = __fmul_rn(x, zh);
+  const float r = __fmaf_rn(-q0, 6.0f, x);
+  const float q = __fmaf_rn(r, zh, q0);
+  return isinf(x) ? x : q;
+}
+
+// Quantise block b of token t (values in a, b2; magnitude max bm).  The
+// block scale is E4M3(max|rn(x*inv)| / 6); rn is monotone, so that max is
+// rn(max|x| * inv).  A block whose scale is 0 keeps zero codes.
+__device__ __forceinline__ void nvfp4_block(const Nvfp4Params& q, const float* s_rcp, int64_t t,
+                                            int64_t b, bool act, uint4 a, uint4 b2, uint32_t bm,
+                                            float inv) {
+  const float braw = absmax2_to_f32(bm);
+  const float bmax = braw > 0.0f ? __fmul_rn(braw, inv) : 0.0f;
+  const uint32_t sc = e4m3x2(div6(bmax), 0.0f) & 0xFFu;
+  const float rs = s_rcp[sc & 0x7Fu];
+  const uint32_t u[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = __fmul_rn(__fmul_rn(bf16_bits_to_f32(u[i] & 0xFFFFu), inv), rs);
+    f[2 * i + 1] = __fmul_rn(__fmul_rn(bf16_bits_to_f32(u[i] >> 16), inv), rs);
+  }
+  uint32_t c0 = e2m1x8(f), c1 = e2m1x8(f + 8);
+  c0 = sc != 0 ? c0 : 0u;
+  c1 = sc != 0 ? c1 : 0u;
+  if (act) {
+    uint32_t* xr = reinterpret_cast<uint32_t*>(q.x + t * q.xs0) + 2 * b;
+    xr[0] = c0;
+    xr[1] = c1;
+    reinterpret_cast<uint8_t*>(q.x_sf + t * q.sfs0)[b] = (uint8_t)sc;  // byte b of the row
+    if (q.shared_x != nullptr) {
+      st_v4(q.shared_x + t * q.shs0 + b * 16, a);
+      st_v4(q.shared_x + t * q.shs0 + b * 16 + 8, b2);
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+  return v;
+}
+
+template <typename IdT, typename WT, int NBL>
+__global__ void __launch_bounds__(128) nvfp4_kernel(Nvfp4Params q, StageParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  // RN(1 / dec(code)) for every E4M3 code of a non-negative scale (0x7F: NaN)
+  __shared__ float s_rcp[128];
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) s_rcp[i] = __frcp_rn(e4m3_to_f32(i));
+  __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
   if (blockIdx.x == 0 && q.l2_alpha != nullptr)
     for (int64_t e = threadIdx.x; e < q.n_local; e += blockDim.x)
       q.l2_alpha[e] = __fmul_rn(q.w2gs[e], q.l2s);
-  const int64_t chunks = q.K / 8;  // a multiple of 16 (K % 128 == 0)
+  const int64_t nb = q.K / 16;  // a multiple of 8 (K % 128 == 0)
   for (int64_t t = gwarp; t < q.T; t += nwarps) {
     const uint16_t* row = q.hidden + t * q.hs0;
-    float amax = 0.0f;
-    if constexpr (REG) {
-      uint4 v[32];
+    if constexpr (NBL > 0) {
+      uint4 va[NBL], vb[NBL];
+      uint32_t bm[NBL];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int64_t c = lane + 32 * i;
-        v[i] = c < chunks ? ld_stream_v4(row + c * 8) : make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < NBL; ++i) {
+        const int64_t b = lane + 32 * i;
+        const bool in = b < nb;
+        va[i] = in ? ld_stream_v4(row + b * 16) : make_uint4(0, 0, 0, 0);
+        vb[i] = in ? ld_stream_v4(row + b * 16 + 8) : make_uint4(0, 0, 0, 0);
       }
+      uint32_t m2 = 0;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, bf16x8_absmax(v[i]));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      for (int i = 0; i < NBL; ++i) {
+        bm[i] = block_absmax2(va[i], vb[i]);
+        m2 = absmax_bf16x2(m2, bm[i]);
+      }
+      const float amax = warp_max(absmax2_to_f32(m2));
       const float xs = __fdiv_rn(amax, 2688.0f);
       if (lane == 0) q.x_scales[t] = xs;
       const float inv = amax > 0.0f ? __frcp_rn(xs) : 0.0f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (32 * i < chunks)  // warp-uniform
-          nvfp4_chunk(q, t, lane + 32 * i, lane + 32 * i < chunks, v[i], inv, lane);
+      for (int i = 0; i < NBL; ++i) {
+        const int64_t b = lane + 32 * i;
+        nvfp4_block(q, s_rcp, t, b, b < nb, va[i], vb[i], bm[i], inv);
       }
     } else {
-      for (int64_t c = lane; c < chunks; c += 32) amax = fmaxf(amax, bf16x8_absmax(ld_stream_v4(row + c * 8)));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      uint32_t m2 = 0;
+      for (int64_t b = lane; b < nb; b += 32)
+        m2 = absmax_bf16x2(m2, block_absmax2(ld_stream_v4(row + b * 16),
+                                             ld_stream_v4(row + b * 16 + 8)));
+      const float amax = warp_max(absmax2_to_f32(m2));
       const float xs = __fdiv_rn(amax, 2688.0f);
       if (lane == 0) q.x_scales[t] = xs;
       const float inv = amax > 0.0f ? __frcp_rn(xs) : 0.0f;
-      for (int64_t c0 = 0; c0 < chunks; c0 += 32) {
-        const int64_t c = c0 + lane;
-        const bool act = c < chunks;
-        const uint4 v = act ? ld_stream_v4(row + c * 8) : make_uint4(0, 0, 0, 0);
-        nvfp4_chunk(q, t, c, act, v, inv, lane);
+      for (int64_t b = lane; b < nb; b += 32) {
+        const uint4 a = ld_stream_v4(row + b * 16), b2 = ld_stream_v4(row + b * 16 + 8);
+        nvfp4_block(q, s_rcp, t, b, true, a, b2, block_absmax2(a, b2), inv);
       }
     }
   }
@@ -798,12 +836,19 @@ moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s) {
 template <typename IdT, typename WT>
 static moe_status_t launch_nvfp4_typed(const moe::Nvfp4Params& q, const StageParams& p,
                                        cudaStream_t s) {
-  auto k = q.K <= 8192 ? moe::nvfp4_kernel<IdT, WT, true> : moe::nvfp4_kernel<IdT, WT, false>;
-  int64_t blocks = (q.T + 7) / 8;
+  // blocks per lane held in registers: the smallest of 4, 8, 14 (hidden 7168),
+  // 16 that fits the row, else the row is streamed twice
+  const int64_t nbl = (q.K / 16 + 31) / 32;
+  auto k = nbl <= 4    ? moe::nvfp4_kernel<IdT, WT, 4>
+           : nbl <= 8  ? moe::nvfp4_kernel<IdT, WT, 8>
+           : nbl <= 14 ? moe::nvfp4_kernel<IdT, WT, 14>
+           : nbl <= 16 ? moe::nvfp4_kernel<IdT, WT, 16>
+                       : moe::nvfp4_kernel<IdT, WT, 0>;
+  int64_t blocks = (q.T + 3) / 4;
   if (blocks < 1) blocks = 1;
-  const int64_t cap = (int64_t)num_sms() * resident_blocks(reinterpret_cast<const void*>(k), 256);
+  const int64_t cap = (int64_t)num_sms() * resident_blocks(reinterpret_cast<const void*>(k), 128);
   if (blocks > cap) blocks = cap;
-  cudaError_t e = launch_pdl(k, dim3((unsigned)blocks), dim3(256), 0, s, q, p);
+  cudaError_t e = launch_pdl(k, dim3((unsigned)blocks), dim3(128), 0, s, q, p);
   if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "nvfp4 launch: %s", cudaGetErrorString(e));
   return MOE_OK;
 }

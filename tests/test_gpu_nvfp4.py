@@ -68,7 +68,10 @@ def _run(hid, ids, w, pad=None, eplb=None, shared=False, n_local=0):
                 status=int(st.item()))
 
 
-@pytest.mark.parametrize("T,K,k", [(37, 640, 3), (64, 256, 2), (200, 7168, 8), (16, 384, 1)])
+# 16-value blocks per lane held in registers: 4 (K <= 2048), 8 (<= 4096),
+# 14 (<= 7168), 16 (<= 8192); K = 9216 streams the row twice
+@pytest.mark.parametrize("T,K,k", [(37, 640, 3), (64, 256, 2), (200, 7168, 8), (16, 384, 1),
+                                   (24, 4096, 2), (12, 8192, 4), (9, 9216, 2)])
 def test_nvfp4_rows_bit_exact(cuda, orc, T, K, k):
     hid = _hidden(T, K, 40 + T)
     ids, w, pad = syn.make_routing(T, 16, k, 41 + T, padding_frac=0.1)
