@@ -3,11 +3,15 @@
 
 One step = the whole path over one batch of synthetic input:
 moe_prepare_inputs (staging + dispatch) -> moe_batched_experts (w13 GEMM with
-fused SiLU-and-mul requant, w2 GEMM) -> moe_topk_reduce.  The default workload
-is the Mixtral-8x7B-shaped decode layer (T=64, K=4096, N=14336, E=8, top-k 2).
+fused SiLU-and-mul requant, w2 GEMM) -> moe_topk_reduce.  The headline
+workload is the largest single-GPU configuration, the DeepSeek-V3-shaped
+prefill layer (T=8192, K=7168, N=2048, E=256, top-8, M_max=1024); the same
+JSON line carries a ``per_config`` block with the Mixtral-8x7B-shaped decode,
+the DeepSeek-V3-shaped decode and the staging-only stress workload (fp8 and
+NVFP4 staging), each with its own time, roofline, end-to-end figure and clocks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config NAME]
+                    [--config NAME] [--no-per-config]
 
 Prints one JSON line.  `value` is TFLOP/s over valid (routed) rows; the
 staging-only workload reports GB/s instead.  Multi-GPU runs (torchrun) are
@@ -16,6 +20,7 @@ independent replicas (weak scaling, no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -32,15 +37,22 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE expert-layer TFLOP/s (valid rows) & staging GB/s, % of FP8/HBM roofline, 1 GB300"
 FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
+L2_NOTE = "inputs larger than L2 and a 512 MB L2 flush before every step"
+HEADLINE = "deepseek_prefill"
+# the other workloads measured in the same run: (workload, staging format)
+PER_CONFIG = [("mixtral_decode", "fp8"), ("deepseek_decode", "fp8"),
+              ("staging_stress", "fp8"), ("staging_stress", "nvfp4")]
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # dominant kernel, from one ncu capture of the committed source; each entry
-# keeps the SHA-256 prefix of that source file and is reported only while the
-# file is unchanged.  The prefill entry is captured on deepseek_prefill_e32
-# (same rows per expert, 1/8 of the experts) and scaled by 8.
+# keeps the SHA-256 prefix of the kernel's source file together with the
+# shared device header, and is reported only while both are unchanged.  The
+# prefill entry is captured on deepseek_prefill_e32 (same rows per expert, 1/8
+# of the experts) and scaled by 8.
 GEMM_SRC = "moe_expert_layer_prepare_gb300/csrc/experts_gemm.cu"
 STAGING_SRC = "moe_expert_layer_prepare_gb300/csrc/staging.cu"
+COMMON_SRC = "moe_expert_layer_prepare_gb300/csrc/common.cuh"
 NCU_TRAFFIC = {
     ("mixtral_decode", "grouped_gemm_kernel<W13>"): (952.31e6, GEMM_SRC, "27b77fc5e84f75d5"),
     ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1040.37e6, GEMM_SRC,
@@ -51,31 +63,39 @@ NCU_TRAFFIC = {
 }
 
 
+def source_key(src):
+    """SHA-256 prefix of a kernel source file and the shared device header."""
+    h = hashlib.sha256()
+    for f in (src, COMMON_SRC):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(workload, kernel):
     ent = NCU_TRAFFIC.get((workload, kernel))
     if ent is None:
         return None
     nbytes, src, sha = ent
-    import hashlib
-    with open(os.path.join(ROOT, src), "rb") as f:
-        cur = hashlib.sha256(f.read()).hexdigest()[:16]
-    return int(nbytes) if cur == sha else None
+    return int(nbytes) if source_key(src) == sha else None
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="mixtral_decode")
+    ap.add_argument("--config", default=HEADLINE)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the --config workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--soak-seconds", type=float, default=1.0)
     ap.add_argument("--stage-format", default="fp8", choices=["fp8", "nvfp4"],
                     help="staging_stress: 1x128 UE8M0 fp8 staging or NVFP4 token staging")
     ap.add_argument("--layout", default="batched", choices=["batched", "contiguous"],
                     help="expert row layout: [E, M_max] slots or expert_offsets")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_setup(args):
@@ -163,9 +183,17 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- workload
-def build_workload(name, device):
+def build_workload(name, device, with_weights=True):
     from moe_expert_layer_prepare_gb300 import synthetic as syn
-    return syn.make_workload(name, weights_device=device)
+    return syn.make_workload(name, weights_device=device, with_weights=with_weights)
+
+
+def routing_counts(wl):
+    c = wl["cfg"]
+    ids = wl["topk_ids"].cpu().numpy()
+    pad = wl["is_padding"].cpu().numpy().astype(bool)
+    routed = ids[~pad]
+    return int(routed.size), int(np.unique(routed).size)
 
 
 def algorithmic(wl):
@@ -178,11 +206,7 @@ def algorithmic(wl):
     """
     c = wl["cfg"]
     T, K, N, E, k = c["T"], c["K"], c["N"], c["E"], c["top_k"]
-    ids = wl["topk_ids"].cpu().numpy()
-    pad = wl["is_padding"].cpu().numpy().astype(bool)
-    routed = ids[~pad]
-    R = int(routed.size)
-    A = int(np.unique(routed).size)
+    R, A = routing_counts(wl)
     G, Gn = K // 128, N // 128
     Wa, Wy = (G + 3) // 4, (Gn + 3) // 4
     w13_bytes = A * (2 * N * K + (2 * N // 128) * G * 4) + R * (K + 4 * Wa) + R * (N + Gn) + 4 * E
@@ -195,7 +219,48 @@ def algorithmic(wl):
                 w13_flops=4.0 * N * K * R, w2_flops=2.0 * N * K * R)
 
 
-def run_oracle_sample(wl, n_tok, seed=0):
+def config_of(name, wl, layout, stage_format, world):
+    """The `config` object of a JSON line; both arms build it here, so that a
+    workload is named identically whichever arm measured it."""
+    c = wl["cfg"]
+    if c.get("N") is None:
+        return dict(workload=name, format=stage_format, T=c["T"], K=c["K"], top_k=c["top_k"],
+                    experts_logical=c["E"], experts_physical=wl["num_physical"], l2=L2_NOTE,
+                    parallelism=f"replicas x{world}")
+    R, A = routing_counts(wl)
+    M_max = max(1, -(-(c["T"] * c["top_k"]) // c["E"])) if layout == "contiguous" else c["M_max"]
+    return dict(workload=name, T=c["T"], K=c["K"], N=c["N"], E=c["E"], top_k=c["top_k"],
+                M_max=M_max, layout=layout, routed_rows=R, active_experts=A, l2=L2_NOTE,
+                parallelism=f"replicas x{world}")
+
+
+def median(xs):
+    return float(np.median(np.asarray(xs, dtype=np.float64)))
+
+
+# ----------------------------------------------------------------- oracle legs
+def _weights_fetcher(wl, cfg_name):
+    """weights_of(experts) for the oracle: the experts' weights as host arrays,
+    from the resident workload tensors when present, else drawn on demand
+    (each expert from its own seeded generator, as in the full set)."""
+    from moe_expert_layer_prepare_gb300 import synthetic as syn
+    c = wl["cfg"]
+
+    def weights_of(experts):
+        if "w13" in wl:
+            sel = torch.as_tensor(np.asarray(experts, np.int64))
+            return tuple(np.ascontiguousarray(wl[n][sel.to(wl[n].device)].cpu().numpy())
+                         for n in ("w13", "w13_s", "w2", "w2_s"))
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        w13, w13_s = syn.make_block_fp8_weights(c["E"], 2 * c["N"], c["K"],
+                                                syn.seed_of(cfg_name, 2), dev, experts=experts)
+        w2, w2_s = syn.make_block_fp8_weights(c["E"], c["K"], c["N"], syn.seed_of(cfg_name, 3),
+                                              dev, experts=experts)
+        return tuple(np.ascontiguousarray(t.cpu().numpy()) for t in (w13, w13_s, w2, w2_s))
+    return weights_of
+
+
+def run_oracle_sample(wl, cfg_name, n_tok, seed=0):
     import oracle
     oracle.build()
     c = wl["cfg"]
@@ -203,16 +268,11 @@ def run_oracle_sample(wl, n_tok, seed=0):
     pad = wl["is_padding"].cpu().numpy()
     cand = np.nonzero(pad == 0)[0]
     tokens = np.sort(rng.choice(cand, size=min(n_tok, cand.size), replace=False))
-
-    def weights_of(experts):
-        sel = torch.as_tensor(np.asarray(experts, np.int64))
-        return tuple(np.ascontiguousarray(wl[n][sel.to(wl[n].device)].cpu().numpy())
-                     for n in ("w13", "w13_s", "w2", "w2_s"))
-
     bits = wl["hidden"].view(torch.int16).numpy().view(np.uint16)
     tm = {}
     oracle.sampled_forward(bits, wl["topk_ids"].numpy(), wl["topk_weights"].numpy(), pad,
-                           c["E"], c["M_max"], c["N"], tokens, weights_of, timings=tm)
+                           c["E"], c["M_max"], c["N"], tokens, _weights_fetcher(wl, cfg_name),
+                           timings=tm)
     return tm, oracle.num_threads(), len(tokens)
 
 
@@ -231,10 +291,24 @@ def run_oracle_staging(wl, n_tok):
     return secs, oracle.num_threads(), n
 
 
-def staging_bytes(T, K, k, wl):
+def run_oracle_nvfp4(wl, n_tok):
+    import oracle
+    oracle.build()
+    K = wl["cfg"]["K"]
+    n = max(1, min(int(n_tok), wl["cfg"]["T"]))
+    bits = wl["hidden"][:n].view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.nvfp4_rows(bits)
+    return time.perf_counter() - t0, oracle.num_threads(), n
+
+
+def staging_bytes(T, K, k, wl, nvfp4=False):
     G = K // 128
-    return T * K * 2 + T * k * 4 * 2 + T * K + T * 4 * ((G + 3) // 4) + T * k * 12 + \
+    b = T * K * 2 + T * k * 4 * 2 + T * K + T * 4 * ((G + 3) // 4) + T * k * 12 + \
         wl["l2p"].numel() * 4 + wl["replica_count"].numel() * 4
+    if nvfp4:  # codes K/2 + E4M3 scales K/16 + fp32 scale, instead of K + K/32
+        b += T * (K // 2 + K // 16 + 4) - T * (K + 4 * ((G + 3) // 4))
+    return b
 
 
 def oracle_tokens_for(wl, seconds):
@@ -243,28 +317,43 @@ def oracle_tokens_for(wl, seconds):
     per_route = 6.0 * c["N"] * c["K"]
     import oracle
     thr = max(oracle.num_threads(), 1)
-    rate = 1.2e8 * thr  # oracle fp64 FLOP/s per thread (measured order of magnitude)
+    rate = 4.0e8 * thr  # oracle fp64 FLOP/s per thread (measured: ~5e8 on Grace cores)
     routes = max(1, int(seconds * rate / per_route))
     return max(1, routes // max(c["top_k"], 1))
 
 
 # ----------------------------------------------------------------- ours
-def bench_ours(args, world, rank, local):
+def timed_steps(step, K, s, nev, flush, world):
+    """K steps, each bracketed by `nev` events (step(evs) records them), an L2
+    flush before every step outside the events.  Returns [K, nev-1] ms."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    return np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(nev - 1)]
+                     for i in range(K)])
+
+
+def soak(step, flush, seconds):
+    t_end = time.time() + seconds
+    while time.time() < t_end:
+        for _ in range(10):
+            flush.zero_()
+            step(None)
+        torch.cuda.synchronize()
+
+
+def bench_experts(name, args, world, dev, peaks, flush, want_cpu):
+    """The whole path on one expert-layer workload."""
     from moe_expert_layer_prepare_gb300 import binding as B
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    B.load()
-    name = args.config
     wl = build_workload(name, dev)
     c = wl["cfg"]
-    peaks = load_peaks()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     s = torch.cuda.current_stream()
-    alg = algorithmic(wl) if c.get("N") else None
-
-    if c.get("N") is None:
-        return bench_staging(args, world, rank, dev, wl, peaks, flush)
-
+    alg = algorithmic(wl)
     layer = B.MoeLayer(c["T"], c["K"], c["N"], c["E"], c["top_k"], c["M_max"], wl["w13"],
                        wl["w13_s"], wl["w2"], wl["w2_s"], device=dev,
                        contiguous=args.layout == "contiguous")
@@ -272,7 +361,7 @@ def bench_ours(args, world, rank, local):
                           wl["topk_weights"].to(dev), wl["is_padding"].to(dev))
     inter_q, inter_sf = layer.inter()
 
-    def step(evs=None):
+    def step(evs):
         if evs:
             evs[0].record(s)
         layer.prepare(hid, ids, wts, pad)
@@ -297,52 +386,33 @@ def bench_ours(args, world, rank, local):
             evs[4].record(s)
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        step(None)
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0, "device status set during warm-up"
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     clocks.start()
-    t_end = time.time() + args.soak_seconds
-    while time.time() < t_end:
-        for _ in range(20):
-            flush.zero_()
-            step()
-        torch.cuda.synchronize()
+    soak(step, flush, args.soak_seconds)
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
-    barrier(world)
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_push("timed")
-    for i in range(K):
-        flush.zero_()  # L2 flush between timed steps (outside the events)
-        step(evs[i])
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_pop()
-    barrier(world)
+    stage_ms = timed_steps(step, K, s, 5, flush, world)
     ck = clocks.stop()
-    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
-                         for i in range(K)])
     step_ms = stage_ms.sum(axis=1)
-    ms = float(step_ms.mean())
-    ms_max = max_over_ranks(world, ms)
-    value = world * alg["flops"] / (ms_max * 1e-3) / 1e12
-    means = stage_ms.mean(axis=0)
-    w13_gbs = alg["w13_bytes"] / (means[1] * 1e-3) / 1e9
-    w13_tfs = alg["w13_flops"] / (means[1] * 1e-3) / 1e12
-    prefill = name == "deepseek_prefill"
-    if prefill:
-        # the GEMM is timed inside a step loop that runs for seconds under the
-        # power cap, so its denominator is the sustained figure (the burst one
-        # is reported beside it)
-        peak = peaks["bf16_sus"] * FP8_OVER_BF16
+    ms = max_over_ranks(world, median(step_ms))
+    value = world * alg["flops"] / (ms * 1e-3) / 1e12
+    med = np.median(stage_ms, axis=0)
+    w13_gbs = alg["w13_bytes"] / (med[1] * 1e-3) / 1e9
+    w13_tfs = alg["w13_flops"] / (med[1] * 1e-3) / 1e12
+    if name == "deepseek_prefill":
+        # tensor-bound: the w13 GEMM against the fp8 burst peak (it runs for
+        # ~2 ms at a time near the boost clock); the fraction of the sustained
+        # figure (a seconds-long GEMM loop at a lower clock) is kept beside it
         burst = peaks["bf16"] * FP8_OVER_BF16
-        roof = dict(bound="tensor", achieved=round(w13_tfs, 2), peak=round(peak, 1),
-                    unit="TFLOP/s", frac=round(w13_tfs / peak, 4),
+        sus = peaks["bf16_sus"] * FP8_OVER_BF16
+        roof = dict(bound="tensor", achieved=round(w13_tfs, 2), peak=round(burst, 1),
+                    unit="TFLOP/s", frac=round(w13_tfs / burst, 4),
                     traffic=ncu_traffic(name, "grouped_gemm_kernel<W13>"),
                     kernel="grouped_gemm_kernel<W13>",
-                    peak_source=f"{peaks['src']} bf16 sustained x {FP8_OVER_BF16} "
-                                f"(fp8/bf16 nominal)",
-                    frac_of_burst=round(w13_tfs / burst, 4), burst_peak=round(burst, 1))
+                    peak_source=f"{peaks['src']} bf16 burst x {FP8_OVER_BF16} (fp8/bf16 nominal)",
+                    frac_of_sustained=round(w13_tfs / sus, 4), sustained_peak=round(sus, 1))
     else:
         roof = dict(bound="hbm", achieved=round(w13_gbs, 1), peak=peaks["hbm"], unit="GB/s",
                     frac=round(w13_gbs / peaks["hbm"], 4),
@@ -358,62 +428,62 @@ def bench_ours(args, world, rank, local):
     for _ in range(3):
         layer.forward_host(hh, ih, wh, ph, oh)
     torch.cuda.synchronize()
-    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(K)]
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(K):
-        e_ev[i][0].record(s)
+
+    def e2e_step(evs):
+        if evs:
+            evs[0].record(s)
         layer.forward_host(hh, ih, wh, ph, oh)
-        e_ev[i][1].record(s)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(world, float(np.mean([a.elapsed_time(b) for a, b in e_ev])))
+        if evs:
+            evs[1].record(s)
+
+    e2e = timed_steps(e2e_step, K, s, 2, flush, world)[:, 0]
+    e2e_ms = max_over_ranks(world, median(e2e))
     h2d = hh.numel() * 2 + ih.numel() * ih.element_size() + wh.numel() * 4 + ph.numel()
     d2h = oh.numel() * 2
     assert int(layer.status.item()) == 0, "device status set during the timed steps"
-
-    out = dict(metric=METRIC, value=round(value, 3), unit="TFLOP/s", n_gpus=world, steps=K,
-               warmup=args.warmup, ms_per_step=round(ms_max, 4), higher_is_better=True,
-               scaling="weak", vs_baseline=None, dtype="fp8e4m3 (fp32 accumulate)",
-               data="synthetic",
-               config=dict(workload=name, T=c["T"], K=c["K"], N=c["N"], E=c["E"],
-                           top_k=c["top_k"], M_max=layer.M_max, layout=args.layout,
-                           routed_rows=alg["R"],
-                           active_experts=alg["A"],
-                           l2="inputs larger than L2 and a 512 MB L2 flush before every step",
-                           parallelism=f"replicas x{world}"),
-               roofline=roof,
-               stages_ms=dict(prepare=round(means[0], 4), w13=round(means[1], 4),
-                              w2=round(means[2], 4), reduce=round(means[3], 4)),
-               stages_gbs=dict(prepare=round(alg["stage_bytes"] / means[0] / 1e6, 1),
+    out = dict(value=round(value, 3), unit="TFLOP/s", ms_per_step=round(ms, 4),
+               dtype="fp8e4m3 (fp32 accumulate)",
+               config=config_of(name, wl, args.layout, "fp8", world), roofline=roof,
+               stages_ms=dict(prepare=round(med[0], 4), w13=round(med[1], 4),
+                              w2=round(med[2], 4), reduce=round(med[3], 4)),
+               stages_gbs=dict(prepare=round(alg["stage_bytes"] / med[0] / 1e6, 1),
                                w13=round(w13_gbs, 1),
-                               w2=round(alg["w2_bytes"] / means[2] / 1e6, 1),
-                               reduce=round(alg["reduce_bytes"] / means[3] / 1e6, 1)),
+                               w2=round(alg["w2_bytes"] / med[2] / 1e6, 1),
+                               reduce=round(alg["reduce_bytes"] / med[3] / 1e6, 1)),
+               stages_tflops=dict(w13=round(w13_tfs, 2),
+                                  w2=round(alg["w2_flops"] / med[2] / 1e9, 2)),
                e2e=dict(value=round(world * alg["flops"] / (e2e_ms * 1e-3) / 1e12, 3),
                         unit="TFLOP/s", h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
                         ms_per_step=round(e2e_ms, 4)),
                gpu_launches=5 * K, clocks=ck)
-    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+    if want_cpu:
         n_tok = oracle_tokens_for(wl, 15.0)
-        tm, thr, ntok = run_oracle_sample(wl, n_tok)
+        tm, thr, ntok = run_oracle_sample(wl, name, n_tok)
         out["cpu_baseline"] = dict(value=round(tm["flops"] / tm["seconds"] / 1e12, 6),
                                    unit="TFLOP/s", cores=thr, kind="oracle",
                                    sample=f"{ntok} tokens ({tm['routes']} routes) of {name}, "
                                           f"{tm['seconds']:.1f} s")
+    del layer
     return out
 
 
-def bench_staging(args, world, rank, dev, wl, peaks, flush):
-    """staging_stress: moe_prepare_inputs alone (token order, EPLB)."""
+def bench_staging(args, world, dev, peaks, flush, want_cpu, fmt):
+    """staging_stress: moe_prepare_inputs (or its NVFP4 form) alone, with EPLB."""
     from moe_expert_layer_prepare_gb300 import binding as B
+    wl = build_workload("staging_stress", dev)
     c = wl["cfg"]
     T, K, k = c["T"], c["K"], c["top_k"]
     G = K // 128
+    nvfp4 = fmt == "nvfp4"
     hid = wl["hidden"].to(dev)
     ids, wts = wl["topk_ids"].to(dev), wl["topk_weights"].to(dev)
-    x = torch.empty((T, K), dtype=torch.uint8, device=dev)
-    x_sf = torch.empty((T, (G + 3) // 4), dtype=torch.int32, device=dev)
+    if nvfp4:
+        x = torch.empty((T, K // 2), dtype=torch.uint8, device=dev)
+        x_sf = torch.empty((T, K // 64), dtype=torch.int32, device=dev)
+        x_scales = torch.empty(T, dtype=torch.float32, device=dev)
+    else:
+        x = torch.empty((T, K), dtype=torch.uint8, device=dev)
+        x_sf = torch.empty((T, (G + 3) // 4), dtype=torch.int32, device=dev)
     io = torch.empty((T, k), dtype=torch.int64, device=dev)
     wo = torch.empty((T, k), dtype=torch.float32, device=dev)
     load = torch.zeros(wl["num_physical"], dtype=torch.int32, device=dev)
@@ -422,64 +492,41 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
                                                                         device=dev),
                 num_unpadded_tokens=torch.tensor([T], dtype=torch.int32, device=dev))
     s = torch.cuda.current_stream()
-    nvfp4 = args.stage_format == "nvfp4"
-    if nvfp4:
-        x = torch.empty((T, K // 2), dtype=torch.uint8, device=dev)
-        x_sf = torch.empty((T, K // 64), dtype=torch.int32, device=dev)
-        x_scales = torch.empty(T, dtype=torch.float32, device=dev)
 
-    def step():
+    def run():
         if nvfp4:
             B.moe_prepare_nvfp4_inputs(hid, ids, wts, x, x_sf, x_scales, io, wo, eplb=eplb)
         else:
             B.moe_prepare_inputs(hid, ids, wts, x, x_sf, io, wo, eplb=eplb)
 
+    def step(evs):
+        if evs:
+            evs[0].record(s)
+        run()
+        if evs:
+            evs[1].record(s)
+
     for _ in range(max(args.warmup, 3)):
-        step()
+        step(None)
     clocks = ClockSampler(dev.index)
     clocks.start()
-    t_end = time.time() + args.soak_seconds
-    while time.time() < t_end:
-        for _ in range(20):
-            flush.zero_()
-            step()
-        torch.cuda.synchronize()
+    soak(step, flush, args.soak_seconds)
     Ks = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(Ks)]
-    barrier(world)
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_push("timed")
-    for i in range(Ks):
-        flush.zero_()
-        evs[i][0].record(s)
-        step()
-        evs[i][1].record(s)
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_pop()
-    barrier(world)
+    t = timed_steps(step, Ks, s, 2, flush, world)[:, 0]
     ck = clocks.stop()
-    ms = max_over_ranks(world, float(np.mean([a.elapsed_time(b) for a, b in evs])))
-    nbytes = staging_bytes(T, K, k, wl)
-    if nvfp4:  # codes K/2 + E4M3 scales K/16 + fp32 scale, instead of K + K/32
-        nbytes += T * (K // 2 + K // 16 + 4) - T * (K + 4 * ((G + 3) // 4))
+    ms = max_over_ranks(world, median(t))
+    nbytes = staging_bytes(T, K, k, wl, nvfp4)
     gbs = world * nbytes / (ms * 1e-3) / 1e9
-    out = dict(metric=METRIC, value=round(gbs, 1), unit="GB/s", n_gpus=world, steps=Ks,
-                warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True,
-                scaling="weak", vs_baseline=None,
-                dtype="bf16->e2m1 (e4m3/16, fp32/token)" if nvfp4 else
-                "bf16->fp8e4m3 (fp32 scale math)",
-                data="synthetic",
-                config=dict(workload="staging_stress", format=args.stage_format, T=T, K=K,
-                            top_k=k, experts_logical=c["E"],
-                            experts_physical=wl["num_physical"],
-                            l2="inputs larger than L2 and a 512 MB L2 flush before every step"),
-                roofline=dict(bound="hbm", achieved=round(gbs / world, 1), peak=peaks["hbm"],
-                              unit="GB/s", frac=round(gbs / world / peaks["hbm"], 4),
-                              traffic=ncu_traffic("staging_stress", "nvfp4_kernel" if nvfp4
-                                                  else "quant_kernel<UE8M0,repack>"),
-                              kernel="nvfp4_kernel" if nvfp4 else "quant_kernel<UE8M0,repack>"),
-                e2e=None, gpu_launches=Ks, clocks=ck)
+    kern = "nvfp4_kernel" if nvfp4 else "quant_kernel<UE8M0,repack>"
+    out = dict(value=round(gbs, 1), unit="GB/s", ms_per_step=round(ms, 4),
+               dtype="bf16->e2m1 (e4m3/16, fp32/token)" if nvfp4 else
+               "bf16->fp8e4m3 (fp32 scale math)",
+               config=config_of("staging_stress", wl, "batched", fmt, world),
+               roofline=dict(bound="hbm", achieved=round(gbs / world, 1), peak=peaks["hbm"],
+                             unit="GB/s", frac=round(gbs / world / peaks["hbm"], 4),
+                             traffic=ncu_traffic("staging_stress", kern), kernel=kern,
+                             peak_source=f"{peaks['src']} hbm_gbs"),
+               gpu_launches=Ks, clocks=ck)
     # end to end: pinned host inputs in, staged outputs back to the host
     hh, ih, wh = (wl["hidden"].pin_memory(), wl["topk_ids"].pin_memory(),
                   wl["topk_weights"].pin_memory())
@@ -489,47 +536,35 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
     ioh = torch.empty((T, k), dtype=torch.int64).pin_memory()
     woh = torch.empty((T, k), dtype=torch.float32).pin_memory()
 
-    def e2e_step():
+    def e2e_step(evs):
+        if evs:
+            evs[0].record(s)
         hid.copy_(hh, non_blocking=True)
         ids.copy_(ih, non_blocking=True)
         wts.copy_(wh, non_blocking=True)
-        step()
+        run()
         xh.copy_(x, non_blocking=True)
         sfh.copy_(x_sf, non_blocking=True)
         if nvfp4:
             xsh.copy_(x_scales, non_blocking=True)
         ioh.copy_(io, non_blocking=True)
         woh.copy_(wo, non_blocking=True)
+        if evs:
+            evs[1].record(s)
 
     for _ in range(3):
-        e2e_step()
+        e2e_step(None)
     torch.cuda.synchronize()
-    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(Ks)]
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(Ks):
-        e_ev[i][0].record(s)
-        e2e_step()
-        e_ev[i][1].record(s)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(world, float(np.mean([a.elapsed_time(b) for a, b in e_ev])))
+    e2e_ms = max_over_ranks(world, median(timed_steps(e2e_step, Ks, s, 2, flush, world)[:, 0]))
     h2d = hh.numel() * 2 + ih.numel() * ih.element_size() + wh.numel() * 4
     d2h = xh.numel() + sfh.numel() * 4 + ioh.numel() * 8 + woh.numel() * 4 + \
         (T * 4 if nvfp4 else 0)
     out["e2e"] = dict(value=round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 1), unit="GB/s",
                       h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
                       ms_per_step=round(e2e_ms, 4))
-    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+    if want_cpu:
         if nvfp4:
-            import oracle
-            oracle.build()
-            n = 2048
-            bits = wl["hidden"][:n].view(torch.int16).numpy().view(np.uint16)
-            t0 = time.perf_counter()
-            oracle.nvfp4_rows(bits)
-            secs, thr = time.perf_counter() - t0, oracle.num_threads()
+            secs, thr, n = run_oracle_nvfp4(wl, 2048)
             nb = n * (K * 2 + K // 2 + K // 16 + 4)
             what = "NVFP4 rows"
         else:
@@ -543,61 +578,99 @@ def bench_staging(args, world, rank, dev, wl, peaks, flush):
     return out
 
 
+def bench_one(name, fmt, args, world, dev, peaks, flush, want_cpu):
+    from moe_expert_layer_prepare_gb300 import synthetic as syn
+    if syn.CONFIGS[name].get("N") is None:
+        r = bench_staging(args, world, dev, peaks, flush, want_cpu, fmt)
+    else:
+        r = bench_experts(name, args, world, dev, peaks, flush, want_cpu)
+    torch.cuda.empty_cache()
+    return r
+
+
+def bench_ours(args, world, rank, local):
+    from moe_expert_layer_prepare_gb300 import binding as B
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B.load()
+    peaks = load_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    want_cpu = world == 1 and rank == 0 and not args.no_cpu_baseline
+    head = bench_one(args.config, args.stage_format, args, world, dev, peaks, flush, want_cpu)
+    out = dict(metric=METRIC, value=head.pop("value"), unit=head.pop("unit"), n_gpus=world,
+               steps=args.steps, warmup=args.warmup, ms_per_step=head.pop("ms_per_step"),
+               higher_is_better=True, scaling="weak", vs_baseline=None, dtype=head.pop("dtype"),
+               data="synthetic", config=head.pop("config"))
+    out.update(head)
+    if not args.no_per_config:
+        per = {}
+        for name, fmt in PER_CONFIG:
+            if name == args.config and fmt == args.stage_format:
+                continue
+            key = name if name != "staging_stress" else f"staging_stress_{fmt}"
+            r = bench_one(name, fmt, args, world, dev, peaks, flush, False)
+            r.pop("gpu_launches", None)
+            per[key] = r
+        out["per_config"] = per
+    return out
+
+
 # ----------------------------------------------------------------- reference
 def bench_reference(args, world, rank):
     """The oracle as it stands on the host cores: each step a bounded sample."""
     if rank != 0:
         return None
-    wl = build_workload(args.config, "cpu")
+    from moe_expert_layer_prepare_gb300 import synthetic as syn
+    staging = syn.CONFIGS[args.config].get("N") is None
+    # expert weights are drawn only for the experts a sample touches
+    wl = build_workload(args.config, "cpu", with_weights=False)
     c = wl["cfg"]
     # each step is a bounded sample so that the whole run stays near 90 s
     per_step_s = max(0.05, min(2.0, 90.0 / max(args.steps + args.warmup, 1)))
-    if c.get("N") is None:
-        return bench_reference_staging(args, world, wl, per_step_s)
-    alg = algorithmic(wl)
+    config = config_of(args.config, wl, args.layout, args.stage_format, world)
+    if staging:
+        return bench_reference_staging(args, world, wl, per_step_s, config)
     n_tok = oracle_tokens_for(wl, per_step_s)
     for _ in range(max(args.warmup, 0)):
-        run_oracle_sample(wl, n_tok, seed=1)
+        run_oracle_sample(wl, args.config, n_tok, seed=1)
     secs, flops = [], []
-    t_wall = time.time()
+    thr = ntok = 0
     for i in range(args.steps):
-        tm, thr, ntok = run_oracle_sample(wl, n_tok, seed=100 + i)
+        tm, thr, ntok = run_oracle_sample(wl, args.config, n_tok, seed=100 + i)
         secs.append(tm["seconds"])
         flops.append(tm["flops"])
     value = sum(flops) / sum(secs) / 1e12
-    ms = 1e3 * float(np.mean(secs))
-    del t_wall
     return dict(metric=METRIC, value=round(value, 6), unit="TFLOP/s", n_gpus=world,
-                steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 3),
+                steps=args.steps, warmup=args.warmup, ms_per_step=round(1e3 * median(secs), 3),
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="fp64 (oracle)",
-                data="synthetic", impl="reference",
-                config=dict(workload=args.config, T=c["T"], K=c["K"], N=c["N"], E=c["E"],
-                            top_k=c["top_k"], M_max=c["M_max"], routed_rows=alg["R"]),
+                data="synthetic", impl="reference", config=config,
                 cpu_baseline=dict(kind="oracle", cores=thr, value=round(value, 6),
                                   sample=f"{ntok} tokens per step of {args.config}"),
                 e2e=dict(value=round(value, 6), unit="TFLOP/s", h2d_bytes_per_step=0,
                          d2h_bytes_per_step=0))
 
 
-def bench_reference_staging(args, world, wl, per_step_s):
+def bench_reference_staging(args, world, wl, per_step_s, config):
     c = wl["cfg"]
     T, K, k = c["T"], c["K"], c["top_k"]
+    nvfp4 = args.stage_format == "nvfp4"
     n_tok = max(1, int(per_step_s * 7000))  # oracle staging runs ~7000 tokens/s (8 threads)
+    fn = run_oracle_nvfp4 if nvfp4 else run_oracle_staging
     for _ in range(max(args.warmup, 0)):
-        run_oracle_staging(wl, n_tok)
+        fn(wl, n_tok)
     secs, nbytes = [], []
     thr = n = 0
     for _ in range(args.steps):
-        sec, thr, n = run_oracle_staging(wl, n_tok)
+        sec, thr, n = fn(wl, n_tok)
         secs.append(sec)
-        nbytes.append(staging_bytes(n, K, k, wl))
+        nbytes.append(n * (K * 2 + K // 2 + K // 16 + 4) if nvfp4 else
+                      staging_bytes(n, K, k, wl))
     value = sum(nbytes) / sum(secs) / 1e9
     return dict(metric=METRIC, value=round(value, 4), unit="GB/s", n_gpus=world,
-                steps=args.steps, warmup=args.warmup, ms_per_step=round(1e3 * np.mean(secs), 3),
+                steps=args.steps, warmup=args.warmup, ms_per_step=round(1e3 * median(secs), 3),
                 higher_is_better=True, scaling="weak", vs_baseline=None,
                 dtype="fp32 group math (oracle)", data="synthetic", impl="reference",
-                config=dict(workload="staging_stress", T=T, K=K, top_k=k,
-                            experts_logical=c["E"], experts_physical=wl["num_physical"]),
+                config=config,
                 cpu_baseline=dict(kind="oracle", cores=thr, value=round(value, 4),
                                   sample=f"first {n} tokens per step of staging_stress"),
                 e2e=dict(value=round(value, 4), unit="GB/s", h2d_bytes_per_step=0,

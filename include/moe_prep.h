@@ -264,10 +264,11 @@ moe_status_t moe_prepare_nvfp4_inputs(const moe_nvfp4_args_t* args, void* stream
 /* MOE_ERR_WORKSPACE before anything is enqueued.  Nothing is allocated: no  */
 /* cudaMalloc/cudaFree or allocating library call.  The array's device       */
 /* address is looked up on the first call made with a device current, so    */
-/* make that first call before any stream capture.  Every call on a device   */
-/* shares the one array and finds the previous call's contents there (each   */
-/* call clears what must start at zero); calls that may overlap on the GPU   */
-/* race on it and must be serialised by the caller.                          */
+/* make that first call before any stream capture (it is looked up again     */
+/* when the device's context has changed, e.g. after cudaDeviceReset).       */
+/* Every call on a device shares the one array and finds the previous call's */
+/* contents there (each call clears what must start at zero); calls that may */
+/* overlap on the GPU race on it and must be serialised by the caller.       */
 /* ------------------------------------------------------------------------ */
 #define MOE_PREPARE_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -224,7 +224,8 @@ moe_status_t moe_batched_experts(const moe_experts_args_t* a, void* stream) {
   if (a->activation != MOE_ACT_SILU)
     return set_error(MOE_ERR_UNSUPPORTED, "only SiLU-and-mul is implemented");
   if (a->a_scale_mode != MOE_SF_UE8M0_PACKED && a->a_scale_mode != MOE_SF_FP32)
-    return set_error(MOE_ERR_UNSUPPORTED, "activation scales must be packed UE8M0");
+    return set_error(MOE_ERR_UNSUPPORTED,
+                     "activation scales must be MOE_SF_UE8M0_PACKED or MOE_SF_FP32");
   const int stages = a->stages == 0 ? MOE_STAGE_ALL : a->stages;
   if (stages < 1 || stages > 3) return set_error(MOE_ERR_INVALID_ARGUMENT, "bad stages mask");
   if (!a->expert_num_tokens) return set_error(MOE_ERR_INVALID_ARGUMENT, "expert_num_tokens is NULL");

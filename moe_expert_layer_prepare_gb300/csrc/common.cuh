@@ -43,11 +43,12 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 // power of two is 2^ceil(log2 a/448) = 2^(E - 135 + [m > 0.75]); the fp32
 // quotient is an exact power of two only when a / 448 is one (448 * 2^k * (1 +
 // d) with 0 < d < 2^-24 is not an fp32 number), so the integer form below gives
-// the same byte for every normal fp32 a without the division.
+// the same byte for every finite fp32 a without the division.  An infinite
+// amax gives an infinite quotient, whose exponent field 255 clamps to 254.
 __device__ __forceinline__ uint32_t ue8m0_exponent(float amax) {
   const uint32_t b = __float_as_uint(fmaxf(amax, 1.0e-4f));
   const uint32_t e = ((b >> 23) & 0xFFu) - 8u + ((b & 0x7FFFFFu) > 0x600000u ? 1u : 0u);
-  return min(max(e, 1u), 254u);
+  return b >= 0x7F800000u ? 254u : min(max(e, 1u), 254u);
 }
 
 // 1 / 2^(e - 127) for an exponent byte in [1, 254] (exact; 2^-127 is subnormal).

@@ -37,6 +37,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -886,6 +887,40 @@ static size_t gemm_smem_bytes() {
          4 * (4 + 2 * moe::MAX_EXPERTS + 8) + 4 * 2 * 2 * moe::BM;
 }
 
+// Per-device set-up of the GEMM kernels: the dynamic shared-memory limit is
+// a per-device function attribute, and the in-kernel register split assumes
+// the launch allocation checked here.  Done once per device, under a lock, so
+// that concurrent first calls and calls on several devices are all covered.
+static moe_status_t prepare_kernels(size_t smem) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return set_error(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ge));
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error(MOE_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return MOE_OK;
+  const void* kernels[3] = {reinterpret_cast<const void*>(moe::grouped_gemm_kernel<true>),
+                            reinterpret_cast<const void*>(moe::grouped_gemm_kernel<false>),
+                            reinterpret_cast<const void*>(moe::grouped_gemm_kernel<true, true>)};
+  for (const void* k : kernels) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "GEMM smem attribute: %s", cudaGetErrorString(e));
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, k) != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "cudaFuncGetAttributes failed for a GEMM kernel");
+    if (fa.numRegs != moe::LAUNCH_REGS)
+      return set_error(MOE_ERR_UNSUPPORTED,
+                       "a GEMM kernel was built with %d registers per thread; the register "
+                       "split needs exactly %d", fa.numRegs, moe::LAUNCH_REGS);
+  }
+  done[dev] = true;
+  return MOE_OK;
+}
+
 moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
   const int64_t E = a->num_experts, M = a->max_tokens_per_expert;
   const int64_t K = a->hidden_size, N = a->intermediate_size;
@@ -916,30 +951,9 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
   }
   const size_t smem = gemm_smem_bytes();
   const int sms = num_sms();
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[0]) {
-    cudaError_t e1 = cudaFuncSetAttribute(moe::grouped_gemm_kernel<true>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaError_t e2 = cudaFuncSetAttribute(moe::grouped_gemm_kernel<false>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaError_t e3 = cudaFuncSetAttribute(moe::grouped_gemm_kernel<true, true>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess)
-      return set_error(MOE_ERR_CUDA, "GEMM smem attribute: %s",
-                       cudaGetErrorString(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3)));
-    // The in-kernel register split assumes the launch allocation below.
-    cudaFuncAttributes fa13, fa2, fa13f;
-    if (cudaFuncGetAttributes(&fa13, moe::grouped_gemm_kernel<true>) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa2, moe::grouped_gemm_kernel<false>) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa13f, moe::grouped_gemm_kernel<true, true>) != cudaSuccess)
-      return set_error(MOE_ERR_CUDA, "cudaFuncGetAttributes failed for the GEMM kernels");
-    if (fa13.numRegs != moe::LAUNCH_REGS || fa2.numRegs != moe::LAUNCH_REGS ||
-        fa13f.numRegs != moe::LAUNCH_REGS)
-      return set_error(MOE_ERR_UNSUPPORTED,
-                       "GEMM kernels built with %d/%d/%d registers per thread; the register "
-                       "split needs exactly %d", fa13.numRegs, fa2.numRegs, fa13f.numRegs,
-                       moe::LAUNCH_REGS);
-    attr_done[0] = true;
+  {
+    moe_status_t st = prepare_kernels(smem);
+    if (st != MOE_OK) return st;
   }
   // Upper bound of the work units: every expert full.  Persistent grid.
   // (the contiguous layout has at most E + E*M/128 m-tiles)

@@ -14,11 +14,15 @@
 // The array exists on every GPU that loads the library, for as long as the
 // process lives.  Its device address is looked up once per device, on the
 // first call made with that device current (so make that first call before
-// any stream capture).  All calls on a device share the one array and it
-// keeps whatever the previous call left in it: the completion counter is
-// cleared by every call (an async memset), the rest is fully rewritten.
+// any stream capture), and again if the device's context has changed since
+// (after a device reset the module is loaded anew, maybe elsewhere).  All
+// calls on a device share the one array and it keeps whatever the previous
+// call left in it: the completion counter is cleared by every call (an async
+// memset), the rest is fully rewritten.
 // Calls that can overlap on the GPU (different streams without ordering)
 // race on the array; serialise them.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -30,7 +34,44 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+  unsigned long long ctx_id;  // context the address belongs to (0: not looked up yet)
+  void* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// Unique id of the calling thread's current context (0 when none is current
+// yet or the driver does not provide the query).  The array's address belongs
+// to the context the module was loaded into: after a device reset the
+// primary context is a new one, and the address is looked up again.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrent)(CUcontext*);
+  typedef CUresult (*GetId)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static bool resolved = false;
+  if (!resolved) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrent>(f1);
+      get_id = reinterpret_cast<GetId>(f2);
+    }
+    resolved = true;
+  }
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 moe_status_t scratch_address(void** out) {
   int dev = -1;
@@ -40,15 +81,19 @@ moe_status_t scratch_address(void** out) {
   if (dev < 0 || dev >= kMaxDevices)
     return moe_host::set_error(MOE_ERR_UNSUPPORTED, "device index %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  unsigned long long ctx = current_context_id();
+  ScratchEntry& ent = g_scratch[dev];
+  if (ent.ptr == nullptr || ctx == 0 || ent.ctx_id != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
     if (e != cudaSuccess || p == nullptr)
       return moe_host::set_error(MOE_ERR_CUDA, "cudaGetSymbolAddress(dispatch scratch): %s",
                                  cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
+    ent.ptr = p;
+    // the lookup makes the primary context current if it was not yet
+    ent.ctx_id = ctx != 0 ? ctx : current_context_id();
   }
-  *out = g_scratch_ptr[dev];
+  *out = ent.ptr;
   return MOE_OK;
 }
 

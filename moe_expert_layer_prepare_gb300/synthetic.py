@@ -102,17 +102,20 @@ def make_routing(T: int, E: int, top_k: int, seed: int, zipf_s: float | None = N
 
 
 def make_block_fp8_weights(E: int, rows: int, cols: int, seed: int, device="cpu",
-                           std: float = 0.02):
+                           std: float = 0.02, experts=None):
     """Static 128x128 block-FP8 expert weights.
 
     Returns (codes uint8 [E, rows, cols], scales fp32 [E, rows/128, cols/128]) on
     `device`.  Each expert is drawn from its own generator so that any expert
-    can be produced alone.
+    can be produced alone: with ``experts`` (a list of expert ids) only those
+    are drawn, stacked in that order, identical to the same experts of the full
+    set on the same device.
     """
     assert rows % 128 == 0 and cols % 128 == 0
-    q = torch.empty((E, rows, cols), dtype=torch.uint8, device=device)
-    s = torch.empty((E, rows // 128, cols // 128), dtype=torch.float32, device=device)
-    for e in range(E):
+    ids = list(range(E)) if experts is None else [int(e) for e in experts]
+    q = torch.empty((len(ids), rows, cols), dtype=torch.uint8, device=device)
+    s = torch.empty((len(ids), rows // 128, cols // 128), dtype=torch.float32, device=device)
+    for i, e in enumerate(ids):
         g = torch.Generator(device=device)
         g.manual_seed(int(seed) * 100003 + e)
         w = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32) * std
@@ -120,8 +123,8 @@ def make_block_fp8_weights(E: int, rows: int, cols: int, seed: int, device="cpu"
         amax = blocks.abs().amax(dim=(1, 3)).clamp_min(1e-12)
         sc = amax / 448.0
         scaled = (blocks / sc[:, None, :, None]).clamp_(-448.0, 448.0)
-        q[e] = scaled.reshape(rows, cols).to(torch.float8_e4m3fn).view(torch.uint8)
-        s[e] = sc
+        q[i] = scaled.reshape(rows, cols).to(torch.float8_e4m3fn).view(torch.uint8)
+        s[i] = sc
     return q, s
 
 

@@ -98,3 +98,57 @@ def oracle_sampled_forward(orc, wl, tokens, want_h=False):
                                wl["topk_weights"].cpu().numpy(),
                                wl["is_padding"].cpu().numpy(), c["E"], c["M_max"], c["N"],
                                tokens, weights_of, want_h=want_h)
+
+
+def coverage_tokens(ids, slots, n_target, seed, tile=128):
+    """A deterministic token sample whose routes reach every m-tile index.
+
+    ids / slots: [T, k] expert ids and within-expert slots (-1 = unrouted).
+    Picks, in order: on the most-loaded expert its first slot, the tile
+    boundaries 127/128/255/256, the first row of its last (ragged) tile and
+    its last slot; on the least-loaded expert its first and last slot; for
+    every m-tile index some expert that has that tile, its first and last
+    row in it; then the last slot of a few random experts; then random
+    tokens up to n_target.  Returns sorted unique token indices.
+    """
+    ids = np.asarray(ids)
+    slots = np.asarray(slots)
+    T, k = ids.shape
+    E = int(ids.max()) + 1
+    counts = np.zeros(E, np.int64)
+    owner = {}
+    for t in range(T):
+        for j in range(k):
+            e, s = int(ids[t, j]), int(slots[t, j])
+            if e >= 0 and s >= 0:
+                owner[(e, s)] = t
+                counts[e] = max(counts[e], s + 1)
+    picks = []
+
+    def take(e, s):
+        if 0 <= s < counts[e] and (e, s) in owner:
+            picks.append(owner[(e, s)])
+
+    heavy = int(np.argmax(counts))
+    n = int(counts[heavy])
+    for s in (0, tile - 1, tile, 2 * tile - 1, 2 * tile, ((n - 1) // tile) * tile, n - 1):
+        take(heavy, s)
+    live = np.nonzero(counts > 0)[0]
+    light = int(live[np.argmin(counts[live])])
+    take(light, 0)
+    take(light, int(counts[light]) - 1)
+    for mt in range(int((counts.max() + tile - 1) // tile)):
+        have = np.nonzero(counts > mt * tile)[0]
+        if have.size:
+            e = int(have[len(have) // 2])
+            take(e, mt * tile)
+            take(e, min(int(counts[e]), (mt + 1) * tile) - 1)
+    rng = np.random.default_rng(seed)
+    for e in rng.choice(live, size=min(6, live.size), replace=False):
+        take(int(e), int(counts[e]) - 1)
+    chosen = list(dict.fromkeys(picks))
+    rest = np.setdiff1d(np.arange(T), chosen)
+    need = max(0, n_target - len(chosen))
+    if need and rest.size:
+        chosen += list(rng.choice(rest, size=min(need, rest.size), replace=False))
+    return np.array(sorted(set(int(t) for t in chosen)), np.int64)

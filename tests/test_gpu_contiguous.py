@@ -13,7 +13,7 @@ import torch
 from moe_expert_layer_prepare_gb300 import binding as B
 from moe_expert_layer_prepare_gb300 import synthetic as syn
 from tests._util import (assert_codes_close, assert_fp_close, bf16_bits, bf16_vals,
-                         need_cuda, oracle_sampled_forward, unpack_exponents)
+                         coverage_tokens, need_cuda, oracle_sampled_forward, unpack_exponents)
 
 pytestmark = pytest.mark.gpu
 
@@ -97,22 +97,52 @@ def test_contiguous_full_path(cuda, orc, T, K, N, E, k, zipf):
 
 def test_contiguous_prefill_full_size(cuda, orc):
     """DeepSeek-V3-shaped prefill (T=8192, E=256, top-8) in the contiguous
-    layout: offsets bit-exact, sampled tokens' outputs against the oracle."""
+    layout: offsets and rows bit-exact; for a deterministic token sample whose
+    routes reach every m-tile index, the tile boundaries 127/128/255/256 and
+    the ragged last tile of the most-loaded expert: h, the requantised w2
+    input, the expert outputs and the token outputs against the oracle."""
     wl = syn.make_workload("deepseek_prefill", weights_device=cuda)
     c = wl["cfg"]
     T, K, N, E, k = c["T"], c["K"], c["N"], c["E"], c["top_k"]
     layer = B.MoeLayer(T, K, N, E, k, None, wl["w13"], wl["w13_s"], wl["w2"], wl["w2_s"],
                        device=cuda, contiguous=True)
-    out = layer.forward(wl["hidden"].to(cuda), wl["topk_ids"].to(cuda),
-                        wl["topk_weights"].to(cuda), wl["is_padding"].to(cuda))
+    h = torch.zeros((E * layer.M_max, 2 * N), dtype=torch.bfloat16, device=cuda)
+    layer.prepare(wl["hidden"].to(cuda), wl["topk_ids"].to(cuda), wl["topk_weights"].to(cuda),
+                  wl["is_padding"].to(cuda))
+    layer.experts(gate_up_dump=h)
+    layer.reduce()
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0
     ids = wl["topk_ids"].numpy().astype(np.int64)
     counts = np.bincount(ids.ravel(), minlength=E)
-    assert np.array_equal(layer.expert_offsets.cpu().numpy(),
-                          np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
-    rng = np.random.default_rng(3)
-    tokens = np.sort(rng.choice(T, 24, replace=False))
-    ref = oracle_sampled_forward(orc, wl, tokens)
-    got = bf16_vals(bf16_bits(out))[tokens]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    assert np.array_equal(layer.expert_offsets.cpu().numpy(), offs)
+    st = orc.prepare_inputs(np.zeros((T, 128), np.uint16), wl["topk_ids"].numpy(),
+                            wl["topk_weights"].numpy(), is_padding=wl["is_padding"].numpy())
+    d = orc.dispatch(st["ids"], np.zeros((T, 128), np.uint8), np.zeros((T, 1), np.int32), E,
+                     c["M_max"], copy_rows=False)
+    rows_gpu = layer.route_slot.cpu().numpy()
+    assert np.array_equal(rows_gpu, np.where(d["route_slot"] >= 0,
+                                             offs[np.maximum(st["ids"], 0)] + d["route_slot"], -1))
+    tokens = coverage_tokens(st["ids"], d["route_slot"], 64, seed=7)
+    ref = oracle_sampled_forward(orc, wl, tokens, want_h=True)
+    g_rows = [int(offs[e]) + s for (i, j, e, s) in ref["routes"]]
+    slots = np.array([s for (i, j, e, s) in ref["routes"]])
+    assert {127, 128, 255, 256} <= set(slots.tolist())
+    assert len(np.unique(slots // 128)) == (int(counts.max()) + 127) // 128
+    idx = torch.as_tensor(g_rows, dtype=torch.int64, device=cuda)
+    cr = np.array([ref["crow_of"][(i, j)] for (i, j, e, s) in ref["routes"]])
+    h_bits = bf16_bits(h[idx])
+    assert_fp_close(bf16_vals(h_bits), bf16_vals(ref["h"][cr]), "prefill h rows (contiguous)")
+    ob = bf16_vals(bf16_bits(layer.out_b.view(-1, K)[idx]))
+    assert_fp_close(ob, bf16_vals(ref["out_b"][cr]), "prefill out_b rows (contiguous)")
+    q_gpu, sf_gpu = layer.inter()
+    yq_ref, ysf_ref = orc.silu_requant_rows(np.arange(len(g_rows)), N, h_bits)
+    eg = unpack_exponents(sf_gpu[idx].cpu().numpy(), N // 128)
+    er = unpack_exponents(ysf_ref, N // 128)
+    assert np.mean(eg == er) > 0.999
+    assert np.all(np.abs(eg.astype(int) - er.astype(int)) <= 1)
+    assert_codes_close(q_gpu[idx].cpu().numpy(), yq_ref, orc.e4m3_decode_table(),
+                       "prefill requant codes (contiguous)")
+    got = bf16_vals(bf16_bits(layer.out))[tokens]
     assert_fp_close(got, bf16_vals(ref["out"]), "prefill output (contiguous, sampled)")

@@ -16,7 +16,7 @@ import torch
 from moe_expert_layer_prepare_gb300 import binding as B
 from moe_expert_layer_prepare_gb300 import synthetic as syn
 from tests._util import (assert_codes_close, assert_fp_close, bf16_bits, bf16_vals,
-                         need_cuda, oracle_sampled_forward, unpack_exponents)
+                         coverage_tokens, need_cuda, oracle_sampled_forward, unpack_exponents)
 
 pytestmark = pytest.mark.gpu
 
@@ -148,35 +148,59 @@ def test_ragged_and_split(cuda, orc, shape):
     assert torch.equal(first, layer.out)
 
 
-@pytest.mark.parametrize("name,n_tok", [("mixtral_decode", 6), ("deepseek_decode", 6),
-                                        ("deepseek_prefill", 4)])
+@pytest.mark.parametrize("name,n_tok", [("mixtral_decode", 16), ("deepseek_decode", 24),
+                                        ("deepseek_prefill", 64)])
 def test_full_size_sampled(cuda, orc, name, n_tok):
-    """Full-size workloads in the bench's launch configuration; the oracle
-    recomputes a sample of tokens (every route of each) one by one."""
+    """Full-size workloads in the bench's launch configuration.  The routing
+    and dispatch are checked over every token; the oracle recomputes a
+    deterministic token sample (every route of each) whose routes reach every
+    m-tile index, the tile boundaries 127/128/255/256 and the ragged last tile
+    of the most-loaded expert.  For those rows: h within the FP tolerance,
+    the requantised w2 input (codes and exponents) against the oracle's
+    SiLU-and-mul + requant of the GPU's own h, expert outputs and token
+    outputs within the FP tolerance."""
     wl = syn.make_workload(name, weights_device="cuda")
     c = wl["cfg"]
     layer = _layer(wl, cuda)
     h = _run_layer(layer, wl, cuda, dump=True)
-    rng = np.random.default_rng(42)
     pad = wl["is_padding"].numpy()
-    cand = np.nonzero(pad == 0)[0]
-    tokens = np.sort(rng.choice(cand, size=n_tok, replace=False))
+    st = orc.prepare_inputs(np.zeros((c["T"], 128), np.uint16), wl["topk_ids"].numpy(),
+                            wl["topk_weights"].numpy(), is_padding=pad)
+    d = orc.dispatch(st["ids"], np.zeros((c["T"], 128), np.uint8),
+                     np.zeros((c["T"], 1), np.int32), c["E"], c["M_max"], copy_rows=False)
+    assert np.array_equal(layer.route_slot.cpu().numpy(), d["route_slot"])
+    assert np.array_equal(layer.expert_num_tokens.cpu().numpy(), d["expert_num_tokens"])
+    tokens = coverage_tokens(st["ids"], d["route_slot"], n_tok, seed=42)
     if pad.any():
-        tokens = np.concatenate([tokens, np.nonzero(pad)[0][:1]])
+        tokens = np.union1d(tokens, np.nonzero(pad)[0][:1])
     ref = oracle_sampled_forward(orc, wl, tokens, want_h=True)
-    assert np.array_equal(layer.route_slot.cpu().numpy(), ref["dispatch"]["route_slot"])
-    assert np.array_equal(layer.expert_num_tokens.cpu().numpy(),
-                          ref["dispatch"]["expert_num_tokens"])
     M, N, K = c["M_max"], c["N"], c["K"]
     g_rows = [e * M + s for (i, j, e, s) in ref["routes"]]
+    slots = np.array([s for (i, j, e, s) in ref["routes"]])
+    assert {127, 128, 255, 256} <= set(slots.tolist()) or M <= 256
+    assert len(np.unique(slots // 128)) == (int(d["expert_num_tokens"].max()) + 127) // 128
     idx = torch.as_tensor(g_rows, dtype=torch.int64, device=cuda)
-    hg = bf16_vals(bf16_bits(h[idx]))
+    h_bits = bf16_bits(h[idx])
+    hg = bf16_vals(h_bits)
     ob = bf16_vals(bf16_bits(layer.out_b.view(-1, K)[idx]))
-    for n_, (i, j, e, s) in enumerate(ref["routes"]):
-        r = ref["crow_of"][(i, j)]
+    cr = np.array([ref["crow_of"][(i, j)] for (i, j, e, s) in ref["routes"]])
+    assert_fp_close(hg, bf16_vals(ref["h"][cr]), f"{name} h rows")
+    assert_fp_close(ob, bf16_vals(ref["out_b"][cr]), f"{name} out_b rows")
+    for n_, r in enumerate(cr):  # row by row as well: no row hides behind the norm
         assert_fp_close(hg[n_], bf16_vals(ref["h"][r]), f"h row {g_rows[n_]}")
         assert_fp_close(ob[n_], bf16_vals(ref["out_b"][r]), f"out_b row {g_rows[n_]}")
+    # requantised w2 input of those rows vs the oracle's S2-S3 on the GPU's own h
+    q_gpu, sf_gpu = layer.inter()
+    yq_ref, ysf_ref = orc.silu_requant_rows(np.arange(len(g_rows)), N, h_bits)
+    Gn = N // 128
+    eg = unpack_exponents(sf_gpu[idx].cpu().numpy(), Gn)
+    er = unpack_exponents(ysf_ref, Gn)
+    assert np.mean(eg == er) > 0.999
+    assert np.all(np.abs(eg.astype(int) - er.astype(int)) <= 1)
+    assert_codes_close(q_gpu[idx].cpu().numpy(), yq_ref, orc.e4m3_decode_table(),
+                       f"{name} requant codes")
     out = bf16_vals(bf16_bits(layer.out))[tokens]
     assert_fp_close(out, bf16_vals(ref["out"]), f"{name} output")
     if pad.any():
-        assert np.all(out[-1] == 0), "padding token must be unrouted"
+        assert np.all(bf16_bits(layer.out)[np.nonzero(pad)[0]] == 0), \
+            "padding tokens must be unrouted"

@@ -89,7 +89,8 @@ def test_nvfp4_rows_bit_exact(cuda, orc, T, K, k):
 
 def test_nvfp4_staging_stress_full_size(cuda, orc):
     """16384 x 7168 with EPLB recording, in one launch: every routing output
-    and the load exactly, and 256 sampled rows of codes and scales."""
+    and the load exactly, and the codes, block scales and row scales of all
+    16384 rows."""
     wl = syn.make_workload("staging_stress")
     c = wl["cfg"]
     T, K = c["T"], c["K"]
@@ -107,11 +108,10 @@ def test_nvfp4_staging_stress_full_size(cuda, orc):
                             num_physical=wl["num_physical"], record_enabled=True)
     assert np.array_equal(g["ids"], rr["ids"]) and np.array_equal(g["w"], rr["weights"])
     assert np.array_equal(load.cpu().numpy(), rr["load"])
-    rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(1).choice(T, 254)]))
-    ref = orc.nvfp4_rows(bf16_bits(wl["hidden"])[rows])
-    _codes_equal(g["x"][rows], ref["x"], orc)
-    assert np.array_equal(g["x_sf"][rows], ref["x_sf"])
-    assert np.array_equal(g["xs"][rows].view(np.int32), ref["x_scales"].view(np.int32))
+    ref = orc.nvfp4_rows(bf16_bits(wl["hidden"]))
+    _codes_equal(g["x"], ref["x"], orc)
+    assert np.array_equal(g["x_sf"], ref["x_sf"])
+    assert np.array_equal(g["xs"].view(np.int32), ref["x_scales"].view(np.int32))
 
 
 def test_nvfp4_l2_alpha_without_tokens(cuda):

@@ -16,7 +16,6 @@ so the comparison is exact, as in the other staging tests.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -105,4 +104,46 @@ def test_noalloc_rejects_oversize(cuda):
     st = lib.moe_prepare_inputs_noalloc(ctypes.byref(a), None)
     assert st == 5
     assert "fixed scratch" in lib.moe_last_error().decode()
-    assert np.isfinite(st)
+
+
+# The largest top-8 problem over 256 experts whose dispatch scratch fits the
+# fixed array: 104,832 tokens need 4,193,536 of its 4,194,304 bytes; one token
+# (eight routes) more needs 4,194,816.
+NEAR_LIMIT_T = 104832
+
+
+def test_noalloc_near_the_limit(cuda):
+    """A problem that fills the fixed array to its last block: the top of the
+    array is used and the result still equals the regular entry point's."""
+    k, E, K = 8, 256, 128
+    assert B.prepare_workspace_size(NEAR_LIMIT_T, k, E) <= 4 << 20
+    assert B.prepare_workspace_size(NEAR_LIMIT_T + 1, k, E) > 4 << 20
+    hid = syn.make_hidden(NEAR_LIMIT_T, K, 21)
+    ids, w, pad = syn.make_routing(NEAR_LIMIT_T, E, k, 22, padding_frac=0.01)
+    M_max = 4096  # every expert's count (about 3,300 routes each) fits
+    got = _stage("noalloc", hid, ids, w, pad, E, M_max)
+    ref = _stage("regular", hid, ids, w, pad, E, M_max)
+    assert int(got["status"].item()) == 0 and int(ref["status"].item()) == 0
+    for name in ref:
+        assert torch.equal(got[name], ref[name]), f"{name} differs at the scratch limit"
+    assert int(ref["ent"].max().item()) < M_max
+
+
+def test_noalloc_refuses_one_token_past_the_limit(cuda):
+    """Eight routes past the boundary are refused on the host."""
+    lib = B.load()
+    a = B.PrepareArgs()
+    fake = 0x10000
+    T, k, K = NEAR_LIMIT_T + 1, 8, 128
+    a.num_tokens, a.hidden_size, a.top_k = T, K, k
+    a.hidden, a.hidden_stride0 = fake, K
+    a.topk_ids, a.topk_ids_stride0, a.topk_ids_stride1 = fake, k, 1
+    a.topk_weights, a.topk_weights_stride0, a.topk_weights_stride1 = fake, k, 1
+    a.x, a.x_stride0 = fake, K
+    a.x_sf, a.sf_mode, a.x_sf_stride0, a.x_sf_stride1 = fake, B.MOE_SF_UE8M0_PACKED, 1, 1
+    a.topk_idx_out, a.topk_idx_out_stride0, a.topk_idx_out_stride1 = fake, k, 1
+    a.topk_weights_out, a.topk_weights_out_stride0, a.topk_weights_out_stride1 = fake, k, 1
+    a.num_experts, a.max_tokens_per_expert = 256, 4096
+    a.x_b, a.sf_b, a.expert_num_tokens, a.route_slot = fake, fake, fake, fake
+    assert lib.moe_prepare_inputs_noalloc(ctypes.byref(a), None) == 5
+    assert "fixed scratch" in lib.moe_last_error().decode()
