@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define MOE_PREP_ABI_VERSION 2
+#define MOE_PREP_ABI_VERSION 3
 
 typedef enum moe_status {
   MOE_OK = 0,
@@ -62,6 +62,7 @@ typedef enum moe_sf_mode {
 typedef enum moe_ids_dtype { MOE_IDS_INT32 = 0, MOE_IDS_INT64 = 1 } moe_ids_dtype_t;
 typedef enum moe_weights_dtype { MOE_WEIGHTS_FP32 = 0, MOE_WEIGHTS_BF16 = 1 } moe_weights_dtype_t;
 typedef enum moe_activation { MOE_ACT_SILU = 0 } moe_activation_t;
+typedef enum moe_shared_dtype { MOE_SHARED_BF16 = 0, MOE_SHARED_FP8 = 1 } moe_shared_dtype_t;
 
 /* Stage mask of moe_batched_experts. */
 #define MOE_STAGE_W13 1
@@ -198,9 +199,17 @@ size_t moe_prepare_workspace_size(int64_t num_tokens, int64_t top_k, int64_t num
 /* nibble of byte i; x_sf: int32 [T, K/64], block b's E4M3 byte at byte     */
 /* b % 4 of word b / 4; x_scales: fp32 [T].                                  */
 /* Routing outputs (topk_idx_out, topk_weights_out, EPLB map and load) are  */
-/* exactly those of moe_prepare_inputs.  shared_x (nullable, bf16 [T, K])    */
-/* receives a copy of the hidden rows (the page's BF16 shared input; its     */
-/* MXFP8 shared input is what moe_prepare_inputs writes with shared_x_sf).  */
+/* exactly those of moe_prepare_inputs.  Shared-expert input (the page's    */
+/* shared_x, nullable), by shared_x_dtype:                                   */
+/*   MOE_SHARED_BF16: bf16 [T, K], a copy of the hidden rows;                */
+/*   MOE_SHARED_FP8 (MXFP8 with shared_x_sf): fp8 e4m3 [T, K], the hidden    */
+/*     rows quantised exactly as moe_prepare_inputs quantises x (1x128        */
+/*     groups, UE8M0 scales), and each group's exponent byte written to      */
+/*     shared_x_sf at row(t) of the shared-expert pages of shared_block_m     */
+/*     (the same layout and row rule as moe_prepare_inputs' shared_x_sf).    */
+/* shared_x_sf and shared_block_m are given exactly for an fp8 shared_x      */
+/* (else INVALID_ARGUMENT, as the page raises); shared_x_sf must hold         */
+/* ceil(T/B)*A rows (SHAPE).                                                 */
 /* l2_alpha[e] = w2_global_scale[e] * l2_activation_scale for e <            */
 /* num_local_experts, written even when T == 0 (both NULL or both given).    */
 /* Errors: K % 128 != 0 -> SHAPE; rows of hidden, x, shared_x not 16-byte    */
@@ -223,8 +232,13 @@ typedef struct moe_nvfp4_args {
   int32_t* x_sf; /* packed E4M3 block scales [T, K/64] */
   int64_t x_sf_stride0;
   float* x_scales; /* [T] */
-  void* shared_x;  /* nullable bf16 [T, K] copy */
+  void* shared_x;  /* nullable: bf16 [T, K] copy, or fp8 [T, K] (shared_x_dtype) */
   int64_t shared_x_stride0;
+  int32_t shared_x_dtype;    /* MOE_SHARED_BF16 or MOE_SHARED_FP8 */
+  uint8_t* shared_x_sf;      /* fp8 shared_x only: UE8M0 bytes [shared_x_sf_rows, K/128] */
+  int64_t shared_x_sf_stride0, shared_x_sf_stride1;
+  int64_t shared_x_sf_rows;
+  int64_t shared_block_m;    /* > 0 iff shared_x_sf != NULL */
   int64_t* topk_idx_out;
   int64_t topk_idx_out_stride0, topk_idx_out_stride1;
   float* topk_weights_out;
@@ -342,7 +356,10 @@ typedef struct moe_experts_args {
   size_t workspace13_bytes;
   void* workspace2;
   size_t workspace2_bytes;
-  int64_t valid_shape_m; /* tuning hint: expected routed rows (T * k); <= 0 = E * M_max */
+  int64_t valid_shape_m; /* tuning hint: the routed rows this call expects, the     */
+                         /* pages' estimate_local_valid_shape_m (T * k, scaled by   */
+                         /* local / global experts); <= 0: this call has no token   */
+                         /* count, so it assumes every row of the layout (E * M_max) */
   void* gate_up_dump;    /* nullable: bf16 [E*M_max, 2N] copy of h (debug/parity) */
   uint32_t* device_status;
 } moe_experts_args_t;
@@ -371,12 +388,18 @@ size_t moe_batched_experts_workspace_size(int64_t num_experts, int64_t max_token
 /* Contiguous layout (moe_unpermute of HummingGroupedExperts.apply): with    */
 /* topk_idx == NULL, route_slot[t, j] is the row of expert_out itself (-1 =  */
 /* unplaced), rows < num_experts * max_tokens_per_expert.                    */
+/* num_valid_tokens (nullable DEVICE int32 scalar; the num_valid_tokens of   */
+/* moe_fused_mul_sum in HummingIndexedExperts.apply): only tokens           */
+/* t < *num_valid_tokens are written, rows past it are left untouched (a     */
+/* negative value writes none).  The launch is sized by num_tokens, so a     */
+/* call captured in a CUDA graph with the largest batch serves every smaller */
+/* batch by updating the scalar.  NULL writes all num_tokens rows.           */
 /* ------------------------------------------------------------------------ */
 moe_status_t moe_topk_reduce(const void* expert_out, int64_t num_experts,
                              int64_t max_tokens_per_expert, int64_t hidden_size,
                              const int64_t* topk_idx, const int32_t* route_slot,
                              const float* topk_weights, int64_t num_tokens, int64_t top_k,
-                             void* out, void* stream);
+                             const int32_t* num_valid_tokens, void* out, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Utilities                                                                 */

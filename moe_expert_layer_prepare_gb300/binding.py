@@ -20,6 +20,7 @@ MOE_SF_NONE, MOE_SF_UE8M0_PACKED, MOE_SF_FP32 = 0, 1, 2
 MOE_IDS_INT32, MOE_IDS_INT64 = 0, 1
 MOE_WEIGHTS_FP32, MOE_WEIGHTS_BF16 = 0, 1
 MOE_ACT_SILU = 0
+MOE_SHARED_BF16, MOE_SHARED_FP8 = 0, 1
 MOE_STAGE_W13, MOE_STAGE_W2, MOE_STAGE_ALL = 1, 2, 3
 MOE_DEV_CAPACITY, MOE_DEV_BAD_EXPERT, MOE_DEV_TIMEOUT = 1, 2, 4
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARGUMENT", 2: "MOE_ERR_SHAPE",
@@ -68,7 +69,9 @@ class Nvfp4Args(ctypes.Structure):
         ("x", _vp), ("x_stride0", _i64),
         ("x_sf", _vp), ("x_sf_stride0", _i64),
         ("x_scales", _vp),
-        ("shared_x", _vp), ("shared_x_stride0", _i64),
+        ("shared_x", _vp), ("shared_x_stride0", _i64), ("shared_x_dtype", _i32),
+        ("shared_x_sf", _vp), ("shared_x_sf_stride0", _i64), ("shared_x_sf_stride1", _i64),
+        ("shared_x_sf_rows", _i64), ("shared_block_m", _i64),
         ("topk_idx_out", _vp), ("topk_idx_out_stride0", _i64), ("topk_idx_out_stride1", _i64),
         ("topk_weights_out", _vp), ("topk_weights_out_stride0", _i64),
         ("topk_weights_out_stride1", _i64),
@@ -106,7 +109,12 @@ def load():
     if not os.path.exists(LIB_PATH):
         raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                            "`python -c 'import __graft_entry__ as g; g.build()'`")
-    lib = ctypes.CDLL(LIB_PATH)
+    _lib = configure(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def configure(lib):
+    """Declare the C signatures on a loaded copy of the library."""
     lib.moe_abi_version.restype = ctypes.c_int
     lib.moe_last_error.restype = ctypes.c_char_p
     lib.moe_prepare_inputs.restype = ctypes.c_int
@@ -121,8 +129,8 @@ def load():
     lib.moe_batched_experts_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _i64,
                                                        ctypes.c_int]
     lib.moe_topk_reduce.restype = ctypes.c_int
-    lib.moe_topk_reduce.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _i64, _vp, _vp]
-    _lib = lib
+    lib.moe_topk_reduce.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _i64, _vp, _vp,
+                                    _vp]
     return lib
 
 
@@ -280,10 +288,13 @@ def moe_prepare_inputs_noalloc(hidden, topk_ids, topk_weights, x, x_sf, topk_idx
 def moe_prepare_nvfp4_inputs(hidden, topk_ids, topk_weights, x, x_sf, x_scales, topk_idx_out,
                              topk_weights_out, is_padding=None, shared_x=None, eplb=None,
                              w2_global_scale=None, l2_alpha=None, l2_activation_scale=1.0,
-                             device_status=None, stream=None):
+                             device_status=None, stream=None, shared_x_sf=None,
+                             shared_block_m=None):
     """NVFP4 token staging (E2M1 + E4M3 per 16 + fp32 per-token scale) and the
     top-k repack.  x: uint8 [T, K/2]; x_sf: int32 [T, K/64]; x_scales: fp32 [T].
-    See include/moe_prep.h."""
+    shared_x: bf16 [T, K] (a copy of the hidden rows) or uint8 [T, K] (the
+    MXFP8 shared input, fp8 codes, given with shared_x_sf uint8 [rows, K/128]
+    and shared_block_m).  See include/moe_prep.h."""
     T, K = hidden.shape
     a = Nvfp4Args()
     a.num_tokens, a.hidden_size = T, K
@@ -303,6 +314,13 @@ def moe_prepare_nvfp4_inputs(hidden, topk_ids, topk_weights, x, x_sf, x_scales, 
     a.x_scales = _ptr(x_scales)
     if shared_x is not None:
         a.shared_x, a.shared_x_stride0 = _ptr(shared_x), shared_x.stride(0)
+        a.shared_x_dtype = MOE_SHARED_BF16 if shared_x.dtype == torch.bfloat16 else MOE_SHARED_FP8
+    if shared_x_sf is not None:
+        a.shared_x_sf = _ptr(shared_x_sf)
+        a.shared_x_sf_stride0, a.shared_x_sf_stride1 = shared_x_sf.stride(0), shared_x_sf.stride(1)
+        a.shared_x_sf_rows = shared_x_sf.shape[0]
+    if shared_block_m is not None:
+        a.shared_block_m = int(shared_block_m)
     a.topk_idx_out = _ptr(topk_idx_out)
     a.topk_idx_out_stride0, a.topk_idx_out_stride1 = topk_idx_out.stride(0), topk_idx_out.stride(1)
     a.topk_weights_out = _ptr(topk_weights_out)
@@ -364,10 +382,13 @@ def moe_batched_experts(output, hidden, a_scale, w13, w13_scale, w2, w2_scale,
     _check("moe_batched_experts", load().moe_batched_experts(ctypes.byref(a), _stream(stream)))
 
 
-def moe_topk_reduce(expert_out, topk_idx, route_slot, topk_weights, out, stream=None):
+def moe_topk_reduce(expert_out, topk_idx, route_slot, topk_weights, out, stream=None,
+                    num_valid_tokens=None):
     """Top-k weighted sum back to token order.  See include/moe_prep.h.
 
     topk_idx None: route_slot holds rows of expert_out (contiguous layout).
+    num_valid_tokens: optional int32 device scalar; tokens at or past it are
+    not written.
     """
     if expert_out.dim() == 3:
         E, M_max, K = expert_out.shape
@@ -376,7 +397,7 @@ def moe_topk_reduce(expert_out, topk_idx, route_slot, topk_weights, out, stream=
     T, k = route_slot.shape
     _check("moe_topk_reduce", load().moe_topk_reduce(
         _ptr(expert_out), E, M_max, K, _ptr(topk_idx), _ptr(route_slot), _ptr(topk_weights), T, k,
-        _ptr(out), _stream(stream)))
+        _ptr(num_valid_tokens), _ptr(out), _stream(stream)))
 
 
 class MoeLayer:

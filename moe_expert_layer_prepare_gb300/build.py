@@ -35,12 +35,12 @@ def _headers_mtime():
     return max(os.path.getmtime(p) for p in paths)
 
 
-def _compile(src, verbose_ptxas=False):
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+def _compile(src, verbose_ptxas=False, build_dir=BUILD_DIR, defines=()):
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     dep = max(os.path.getmtime(src), _headers_mtime())
     if os.path.exists(obj) and os.path.getmtime(obj) >= dep and not verbose_ptxas:
         return obj, ""
-    cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
+    cmd = [NVCC, *ARCH, *FLAGS, *[f"-D{d}" for d in defines], "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -70,6 +70,33 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB_PATH)
     return LIB_PATH
+
+
+# Test-only builds of the library with compile-time knobs (for example the
+# failure-detection test's shortened wait limit and withheld pipeline stage).
+# They go to their own folder and file name; build() above never uses them.
+TEST_VARIANTS = {
+    "timeout": ("MOE_WAIT_LIMIT_NS=5000000ull", "MOE_TEST_WITHHOLD_STAGE"),
+}
+
+
+def build_test_variant(name: str) -> str:
+    defines = TEST_VARIANTS[name]
+    bdir = os.path.join(BUILD_DIR, "test_" + name)
+    os.makedirs(bdir, exist_ok=True)
+    srcs = sources()
+    with ThreadPoolExecutor(max_workers=len(srcs)) as ex:
+        objs = [o for o, _ in ex.map(lambda s: _compile(s, False, bdir, defines), srcs)]
+    lib = os.path.join(bdir, f"libmoe_prep_test_{name}.so")
+    newest = max(os.path.getmtime(o) for o in objs)
+    if not os.path.exists(lib) or os.path.getmtime(lib) < newest:
+        tmp = lib + f".tmp{os.getpid()}"
+        r = subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True,
+                           text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -55,7 +55,8 @@ moe_status_t launch_prepare(const moe_prepare_args_t* a, cudaStream_t s);
 moe_status_t launch_nvfp4(const moe_nvfp4_args_t* a, cudaStream_t s);
 moe_status_t launch_topk_reduce(const void* expert_out, int64_t E, int64_t M_max, int64_t K,
                                 const int64_t* idx, const int32_t* slot, const float* w,
-                                int64_t T, int64_t top_k, void* out, cudaStream_t s);
+                                int64_t T, int64_t top_k, const int32_t* num_valid, void* out,
+                                cudaStream_t s);
 size_t experts_workspace_size(int64_t E, int64_t M_max, int64_t K, int64_t N,
                               int64_t valid_shape_m, int which);
 moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s);
@@ -170,10 +171,32 @@ moe_status_t moe_prepare_nvfp4_inputs(const moe_nvfp4_args_t* a, void* stream) {
     return set_error(MOE_ERR_INVALID_ARGUMENT, "w2_global_scale and l2_alpha go together");
   if (a->l2_alpha != nullptr && a->num_local_experts == 0)
     return set_error(MOE_ERR_INVALID_ARGUMENT, "l2_alpha needs num_local_experts > 0");
+  if (a->shared_x_dtype != MOE_SHARED_BF16 && a->shared_x_dtype != MOE_SHARED_FP8)
+    return set_error(MOE_ERR_INVALID_ARGUMENT, "bad shared_x_dtype %d", a->shared_x_dtype);
+  {
+    // the page: shared_x_sf and shared_block_m are given exactly for an fp8 shared_x
+    const bool fp8_shared = a->shared_x != nullptr && a->shared_x_dtype == MOE_SHARED_FP8;
+    if (fp8_shared != (a->shared_x_sf != nullptr) ||
+        (a->shared_x_sf == nullptr) != (a->shared_block_m == 0))
+      return set_error(MOE_ERR_INVALID_ARGUMENT,
+                       "NVFP4 staging needs shared_x_sf and shared_block_m exactly for an fp8 "
+                       "shared_x");
+  }
   if (a->num_tokens == 0 && a->l2_alpha == nullptr) return MOE_OK;
   if (a->hidden_size % 128 != 0)
     return set_error(MOE_ERR_SHAPE, "hidden_size %lld is not a multiple of 128",
                      (long long)a->hidden_size);
+  if (a->shared_x_sf != nullptr && a->num_tokens > 0) {
+    if (a->shared_block_m < 0)
+      return set_error(MOE_ERR_INVALID_ARGUMENT, "shared_block_m must be positive");
+    const int64_t aligned = (a->shared_block_m + 127) / 128 * 128;
+    const int64_t need = (a->num_tokens + a->shared_block_m - 1) / a->shared_block_m * aligned;
+    if (a->shared_x_sf_rows < need)
+      return set_error(MOE_ERR_SHAPE, "shared_x_sf needs %lld rows, got %lld", (long long)need,
+                       (long long)a->shared_x_sf_rows);
+    if (a->shared_x_sf_stride0 < 1 || (a->hidden_size > 128 && a->shared_x_sf_stride1 < 1))
+      return set_error(MOE_ERR_SHAPE, "shared_x_sf strides must be positive");
+  }
   if (a->num_tokens > 0) {
     if (a->top_k < 1) return set_error(MOE_ERR_SHAPE, "top_k must be >= 1");
     if (a->topk_ids_dtype != MOE_IDS_INT32 && a->topk_ids_dtype != MOE_IDS_INT64)
@@ -187,10 +210,11 @@ moe_status_t moe_prepare_nvfp4_inputs(const moe_nvfp4_args_t* a, void* stream) {
     if (a->hidden_stride0 < K || a->x_stride0 < K / 2 || a->x_sf_stride0 < K / 64 ||
         (a->shared_x != nullptr && a->shared_x_stride0 < K))
       return set_error(MOE_ERR_SHAPE, "row stride smaller than the row");
+    const int64_t shared_elem = a->shared_x_dtype == MOE_SHARED_FP8 ? 1 : 2;
     if (!aligned16(a->hidden) || (a->hidden_stride0 * 2) % 16 != 0 ||
         (reinterpret_cast<uintptr_t>(a->x) & 3u) != 0 || a->x_stride0 % 4 != 0 ||
         (a->shared_x != nullptr &&
-         (!aligned16(a->shared_x) || (a->shared_x_stride0 * 2) % 16 != 0)))
+         (!aligned16(a->shared_x) || (a->shared_x_stride0 * shared_elem) % 16 != 0)))
       return set_error(MOE_ERR_ALIGNMENT, "hidden/shared_x rows must start on 16-byte and x "
                                           "rows on 4-byte boundaries");
     if (a->logical_to_physical != nullptr &&
@@ -272,7 +296,7 @@ moe_status_t moe_topk_reduce(const void* expert_out, int64_t num_experts,
                              int64_t max_tokens_per_expert, int64_t hidden_size,
                              const int64_t* topk_idx, const int32_t* route_slot,
                              const float* topk_weights, int64_t num_tokens, int64_t top_k,
-                             void* out, void* stream) {
+                             const int32_t* num_valid_tokens, void* out, void* stream) {
   g_last_error[0] = '\0';
   if (num_tokens < 0 || top_k < 0 || hidden_size < 0)
     return set_error(MOE_ERR_INVALID_ARGUMENT, "negative size");
@@ -288,8 +312,8 @@ moe_status_t moe_topk_reduce(const void* expert_out, int64_t num_experts,
   if (!aligned16(expert_out) || !aligned16(out))
     return set_error(MOE_ERR_ALIGNMENT, "expert_out and out must be 16-byte aligned");
   return launch_topk_reduce(expert_out, num_experts, max_tokens_per_expert, hidden_size,
-                            topk_idx, route_slot, topk_weights, num_tokens, top_k, out,
-                            static_cast<cudaStream_t>(stream));
+                            topk_idx, route_slot, topk_weights, num_tokens, top_k,
+                            num_valid_tokens, out, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

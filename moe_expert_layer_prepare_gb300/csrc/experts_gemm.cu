@@ -128,7 +128,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: false when the CTA aborted or this wait exceeded ~2 s.
+// Limit of one pipeline wait in nanoseconds (2 s; the timeout test's build
+// shortens it).
+#ifndef MOE_WAIT_LIMIT_NS
+#define MOE_WAIT_LIMIT_NS 2000000000ull
+#endif
+
+// Bounded wait: false when the CTA aborted or this wait exceeded the limit.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -137,7 +143,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > 2000000000ull) {
+      if (globaltimer() - t0 > (uint64_t)MOE_WAIT_LIMIT_NS) {
         *abort_flag = 1;
         set_status(status, MOE_DEV_TIMEOUT);
         return false;
@@ -452,16 +458,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          if (elect_one()) {
-            mbar_expect_tx(fb, tx);
-            for (int i = 0; i < n_boxes; ++i)
-              tma_load_2d(sa + i * A_BOX_ROWS * BK, &tmA, kb * BK, a_row0 + i * A_BOX_ROWS, fb);
-            tma_load_2d(sb, &tmB, kb * BK, b_row0, fb);
-            tma_load_2d(sb + 128 * BK, &tmB, kb * BK, b_row1, fb);
+#ifdef MOE_TEST_WITHHOLD_STAGE
+          // Failure-detection test builds only (the library build never sets
+          // this): CTA 0 withholds the third stage of its first unit -- no
+          // expect_tx and no copy, so no copy is ever left in flight -- and
+          // the MMA warp's bounded wait on that stage runs out.
+          const bool withhold = blockIdx.x == 0 && u == (int)blockIdx.x && kb == w.kb0 + 2;
+#else
+          constexpr bool withhold = false;
+#endif
+          if (!withhold) {
+            if (elect_one()) {
+              mbar_expect_tx(fb, tx);
+              for (int i = 0; i < n_boxes; ++i)
+                tma_load_2d(sa + i * A_BOX_ROWS * BK, &tmA, kb * BK, a_row0 + i * A_BOX_ROWS, fb);
+              tma_load_2d(sb, &tmB, kb * BK, b_row0, fb);
+              tma_load_2d(sb + 128 * BK, &tmB, kb * BK, b_row1, fb);
+            }
+            __syncwarp();
+            issued_mask |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           }
-          __syncwarp();
-          issued_mask |= 1u << stage;
-          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;

@@ -10,7 +10,9 @@
 // route) and the routed expert rows are read eight at a time with streaming
 // 16-byte loads, then weighted in fp32 and accumulated in ascending j; one
 // bf16 rounding at the end.  HBM-bound: each routed row is read once, each output row
-// written once.
+// written once.  An optional device scalar bounds the tokens written
+// (moe_fused_mul_sum's num_valid_tokens), so that one launch configuration,
+// captured in a graph, serves every smaller batch.
 #include "common.cuh"
 
 namespace moe {
@@ -22,7 +24,8 @@ struct ReduceParams {
   const int32_t* slot;   // [T, k]
   const float* w;        // [T, k]
   int64_t T, top_k;
-  uint16_t* out;         // bf16 [T, K]
+  const int32_t* num_valid;  // nullable device scalar: tokens >= *num_valid are not written
+  uint16_t* out;             // bf16 [T, K]
 };
 
 // Row of route j of token t in expert_out, or -1 when the route is unrouted
@@ -44,9 +47,15 @@ __global__ void __launch_bounds__(256) topk_reduce_kernel(ReduceParams p) {
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   // tasks index (token, 256-column chunk) pairs; the host keeps T * chunks < 2^31
   const uint32_t chunks = (uint32_t)((p.K + 255) / 256);
-  const uint32_t tasks = (uint32_t)(p.T * chunks);
   pdl_wait();
   pdl_launch_dependents();
+  // the device-side token bound (a captured graph can run smaller batches)
+  int64_t T = p.T;
+  if (p.num_valid != nullptr) {
+    const int64_t nv = *p.num_valid;
+    T = nv < 0 ? 0 : (nv < T ? nv : T);
+  }
+  const uint32_t tasks = (uint32_t)(T * chunks);
   for (uint32_t task = (uint32_t)gwarp; task < tasks; task += (uint32_t)nwarps) {
     const uint32_t tq = task / chunks;
     const int64_t t = tq;
@@ -108,9 +117,10 @@ namespace moe_host {
 
 moe_status_t launch_topk_reduce(const void* expert_out, int64_t E, int64_t M_max, int64_t K,
                                 const int64_t* idx, const int32_t* slot, const float* w,
-                                int64_t T, int64_t top_k, void* out, cudaStream_t s) {
+                                int64_t T, int64_t top_k, const int32_t* num_valid, void* out,
+                                cudaStream_t s) {
   moe::ReduceParams p{static_cast<const uint16_t*>(expert_out), E, M_max, K, idx, slot, w, T,
-                      top_k, static_cast<uint16_t*>(out)};
+                      top_k, num_valid, static_cast<uint16_t*>(out)};
   const int64_t tasks = T * ((K + 255) / 256);
   int64_t blocks = (tasks * 32 + 255) / 256;
   const int64_t cap =

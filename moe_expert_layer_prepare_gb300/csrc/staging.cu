@@ -22,6 +22,7 @@
 //                  of x_b.
 //                  Without dispatch the repack is folded into this kernel.
 #include <cstdio>
+#include <type_traits>
 
 #include <cuda_fp16.h>
 
@@ -504,8 +505,11 @@ struct Nvfp4Params {
   uint32_t* x_sf;
   int64_t sfs0;
   float* x_scales;
-  uint16_t* shared_x;
-  int64_t shs0;
+  uint16_t* shared_x;   // bf16 copy (MOE_SHARED_BF16)
+  uint8_t* shared_q;    // fp8 MXFP8 shared input (MOE_SHARED_FP8)
+  int64_t shs0;         // row stride of either, in its elements
+  uint8_t* shared_sf;   // fp8 shared input: exponent bytes of the shared-expert pages
+  int64_t ss0, ss1, sbm, sbm_aligned;
   const float* w2gs;
   float* l2_alpha;
   int64_t n_local;
@@ -598,13 +602,47 @@ __device__ __forceinline__ void nvfp4_block(const Nvfp4Params& q, const float* s
   }
 }
 
+// The MXFP8 shared input of one 16-value block: the 1x128 group of block b
+// is the 8 consecutive blocks 8g..8g+7, held by 8 consecutive lanes of the
+// same register slot, so the group amax is a max over those 8 lanes of the
+// blocks' magnitude maxima.  Codes and the exponent byte follow the fp8
+// staging recipe (UE8M0 power of two, x * (1/qs) rounded to e4m3).  Every
+// lane of the warp must call this (the groups of 8 lanes are either wholly
+// inside the row or wholly past it).
+__device__ __forceinline__ void shared_fp8_block(const Nvfp4Params& q, int64_t t, int64_t b,
+                                                 bool act, uint4 a, uint4 b2, uint32_t bm) {
+  float gm = absmax2_to_f32(bm);
+  gm = fmaxf(gm, __shfl_xor_sync(0xFFFFFFFFu, gm, 1));
+  gm = fmaxf(gm, __shfl_xor_sync(0xFFFFFFFFu, gm, 2));
+  gm = fmaxf(gm, __shfl_xor_sync(0xFFFFFFFFu, gm, 4));
+  const uint32_t code = ue8m0_exponent(gm);
+  const float inv = ue8m0_inverse(code);
+  if (act) {
+    const uint32_t u[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = pack4_e4m3(__fmul_rn(bf16_bits_to_f32(u[2 * i] & 0xFFFFu), inv),
+                        __fmul_rn(bf16_bits_to_f32(u[2 * i] >> 16), inv),
+                        __fmul_rn(bf16_bits_to_f32(u[2 * i + 1] & 0xFFFFu), inv),
+                        __fmul_rn(bf16_bits_to_f32(u[2 * i + 1] >> 16), inv));
+    st_v4(q.shared_q + t * q.shs0 + b * 16, make_uint4(o[0], o[1], o[2], o[3]));
+    if ((threadIdx.x & 7) == 0) {
+      const int64_t m = t % q.sbm;
+      const int64_t row = (t / q.sbm) * q.sbm_aligned + (m / 128) * 128 + (m % 32) * 4 +
+                          (m % 128) / 32;
+      q.shared_sf[row * q.ss0 + (b >> 3) * q.ss1] = (uint8_t)code;
+    }
+  }
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
   return v;
 }
 
-template <typename IdT, typename WT, int NBL>
+template <typename IdT, typename WT, int NBL, bool SHARED_FP8>
 __global__ void __launch_bounds__(128) nvfp4_kernel(Nvfp4Params q, StageParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -645,6 +683,7 @@ __global__ void __launch_bounds__(128) nvfp4_kernel(Nvfp4Params q, StageParams p
       for (int i = 0; i < NBL; ++i) {
         const int64_t b = lane + 32 * i;
         nvfp4_block(q, s_rcp, t, b, b < nb, va[i], vb[i], bm[i], inv);
+        if constexpr (SHARED_FP8) shared_fp8_block(q, t, b, b < nb, va[i], vb[i], bm[i]);
       }
     } else {
       uint32_t m2 = 0;
@@ -655,9 +694,15 @@ __global__ void __launch_bounds__(128) nvfp4_kernel(Nvfp4Params q, StageParams p
       const float xs = __fdiv_rn(amax, 2688.0f);
       if (lane == 0) q.x_scales[t] = xs;
       const float inv = amax > 0.0f ? __frcp_rn(xs) : 0.0f;
-      for (int64_t b = lane; b < nb; b += 32) {
-        const uint4 a = ld_stream_v4(row + b * 16), b2 = ld_stream_v4(row + b * 16 + 8);
-        nvfp4_block(q, s_rcp, t, b, true, a, b2, block_absmax2(a, b2), inv);
+      // warp-uniform trip count: the shared input's group max is a shuffle
+      for (int64_t b0 = 0; b0 < nb; b0 += 32) {
+        const int64_t b = b0 + lane;
+        const bool act = b < nb;
+        const uint4 a = act ? ld_stream_v4(row + b * 16) : make_uint4(0, 0, 0, 0);
+        const uint4 b2 = act ? ld_stream_v4(row + b * 16 + 8) : make_uint4(0, 0, 0, 0);
+        const uint32_t bmx = block_absmax2(a, b2);
+        nvfp4_block(q, s_rcp, t, b, act, a, b2, bmx, inv);
+        if constexpr (SHARED_FP8) shared_fp8_block(q, t, b, act, a, b2, bmx);
       }
     }
   }
@@ -839,11 +884,15 @@ static moe_status_t launch_nvfp4_typed(const moe::Nvfp4Params& q, const StagePar
   // blocks per lane held in registers: the smallest of 4, 8, 14 (hidden 7168),
   // 16 that fits the row, else the row is streamed twice
   const int64_t nbl = (q.K / 16 + 31) / 32;
-  auto k = nbl <= 4    ? moe::nvfp4_kernel<IdT, WT, 4>
-           : nbl <= 8  ? moe::nvfp4_kernel<IdT, WT, 8>
-           : nbl <= 14 ? moe::nvfp4_kernel<IdT, WT, 14>
-           : nbl <= 16 ? moe::nvfp4_kernel<IdT, WT, 16>
-                       : moe::nvfp4_kernel<IdT, WT, 0>;
+  auto pick = [&](auto fp8) {
+    constexpr bool F = decltype(fp8)::value;
+    return nbl <= 4    ? moe::nvfp4_kernel<IdT, WT, 4, F>
+           : nbl <= 8  ? moe::nvfp4_kernel<IdT, WT, 8, F>
+           : nbl <= 14 ? moe::nvfp4_kernel<IdT, WT, 14, F>
+           : nbl <= 16 ? moe::nvfp4_kernel<IdT, WT, 16, F>
+                       : moe::nvfp4_kernel<IdT, WT, 0, F>;
+  };
+  auto k = q.shared_q != nullptr ? pick(std::true_type{}) : pick(std::false_type{});
   int64_t blocks = (q.T + 3) / 4;
   if (blocks < 1) blocks = 1;
   const int64_t cap = (int64_t)num_sms() * resident_blocks(reinterpret_cast<const void*>(k), 128);
@@ -864,8 +913,15 @@ moe_status_t launch_nvfp4(const moe_nvfp4_args_t* a, cudaStream_t s) {
   q.x_sf = reinterpret_cast<uint32_t*>(a->x_sf);
   q.sfs0 = a->x_sf_stride0;
   q.x_scales = a->x_scales;
-  q.shared_x = static_cast<uint16_t*>(a->shared_x);
+  const bool fp8_shared = a->shared_x_dtype == MOE_SHARED_FP8;
+  q.shared_x = fp8_shared ? nullptr : static_cast<uint16_t*>(a->shared_x);
+  q.shared_q = fp8_shared ? static_cast<uint8_t*>(a->shared_x) : nullptr;
   q.shs0 = a->shared_x_stride0;
+  q.shared_sf = a->shared_x_sf;
+  q.ss0 = a->shared_x_sf_stride0;
+  q.ss1 = a->shared_x_sf_stride1;
+  q.sbm = a->shared_block_m > 0 ? a->shared_block_m : 1;
+  q.sbm_aligned = (q.sbm + 127) / 128 * 128;
   q.w2gs = a->w2_global_scale;
   q.l2_alpha = a->l2_alpha;
   q.n_local = a->num_local_experts;

@@ -92,7 +92,7 @@ def _load():
         lib.orc_w2_rows.restype = None
         lib.orc_w2_rows.argtypes = [i64, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp]
         lib.orc_topk_reduce.restype = None
-        lib.orc_topk_reduce.argtypes = [i64, i64, i64, i64, vp, vp, vp, vp, vp]
+        lib.orc_topk_reduce.argtypes = [i64, i64, i64, i64, vp, vp, vp, vp, vp, i64]
         _lib = lib
         return lib
 
@@ -340,8 +340,11 @@ def w2_rows(rows, M_max, K, N, y_q, y_sf, w2, w2_s, row_expert=None):
 
 
 # --------------------------------------------------------------------------- S8
-def topk_reduce(out_b_bits, ids, route_slot, weights, M_max):
-    """S8.  ids None: route_slot holds the rows (contiguous layout)."""
+def topk_reduce(out_b_bits, ids, route_slot, weights, M_max, num_valid=None, fill=0):
+    """S8.  ids None: route_slot holds the rows (contiguous layout).
+
+    num_valid: rows t >= num_valid are not written (they keep ``fill``);
+    None = every token."""
     lib = _load()
     out_b = _c(out_b_bits, np.uint16)
     ids = None if ids is None else _c(ids, np.int64)
@@ -349,8 +352,9 @@ def topk_reduce(out_b_bits, ids, route_slot, weights, M_max):
     w = _c(weights, np.float32)
     T, top_k = slot.shape
     K = out_b.shape[-1]
-    out = np.zeros((T, K), np.uint16)
-    lib.orc_topk_reduce(T, top_k, K, M_max, _p(out_b), _p(ids), _p(slot), _p(w), _p(out))
+    out = np.full((T, K), fill, np.uint16)
+    lib.orc_topk_reduce(T, top_k, K, M_max, _p(out_b), _p(ids), _p(slot), _p(w), _p(out),
+                        -1 if num_valid is None else int(num_valid))
     return out
 
 

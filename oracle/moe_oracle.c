@@ -505,12 +505,16 @@ void orc_w2_rows(int64_t n_rows, const int64_t* rows, int64_t M_max, int64_t K, 
 /* S8: top-k weighted reduce back to token order.                            */
 /* out[t, c] = bf16( sum_{j: slot >= 0} w[t,j] * out_b[id, slot, c] ), j     */
 /* ascending; tokens without a placed route give zeros.                      */
+/* num_valid (moe_fused_mul_sum's num_valid_tokens on the experts page, a   */
+/* device scalar there): rows t >= num_valid are not written; a negative     */
+/* value means every token.                                                  */
 /* ------------------------------------------------------------------------ */
 void orc_topk_reduce(int64_t T, int64_t top_k, int64_t K, int64_t M_max, const uint16_t* out_b,
                      const int64_t* ids, const int32_t* route_slot, const float* w,
-                     uint16_t* out) {
+                     uint16_t* out, int64_t num_valid) {
+  const int64_t bound = num_valid < 0 ? T : (num_valid < T ? num_valid : T);
 #pragma omp parallel for schedule(static)
-  for (int64_t t = 0; t < T; ++t) {
+  for (int64_t t = 0; t < bound; ++t) {
     for (int64_t c = 0; c < K; ++c) {
       double acc = 0.0;
       for (int64_t j = 0; j < top_k; ++j) {

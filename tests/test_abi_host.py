@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
         assert must in names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/moe_prep.h but not exported"
-    assert lib.moe_abi_version() == 2
+    assert lib.moe_abi_version() == 3
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails its checks first
@@ -137,10 +137,10 @@ def test_experts_rejects(lib):
 
 def test_reduce_rejects(lib):
     f = lib.moe_topk_reduce
-    assert f(FAKE, 4, 8, 100, FAKE, FAKE, FAKE, 4, 2, FAKE, None) == 2
-    assert f(None, 4, 8, 256, FAKE, FAKE, FAKE, 4, 2, FAKE, None) == 1
-    assert f(FAKE + 2, 4, 8, 256, FAKE, FAKE, FAKE, 4, 2, FAKE, None) == 4
-    assert f(FAKE, 4, 8, 256, FAKE, FAKE, FAKE, 0, 2, FAKE, None) == 0
+    assert f(FAKE, 4, 8, 100, FAKE, FAKE, FAKE, 4, 2, None, FAKE, None) == 2
+    assert f(None, 4, 8, 256, FAKE, FAKE, FAKE, 4, 2, None, FAKE, None) == 1
+    assert f(FAKE + 2, 4, 8, 256, FAKE, FAKE, FAKE, 4, 2, None, FAKE, None) == 4
+    assert f(FAKE, 4, 8, 256, FAKE, FAKE, FAKE, 0, 2, FAKE, FAKE, None) == 0
 
 
 def test_workspace_sizes(lib):
@@ -175,3 +175,16 @@ def test_nvfp4_rejects(lib):
     assert run(args(x_sf_stride0=3)) == 2                  # K/64 = 4 words per row
     assert run(args(top_k=0)) == 2
     assert run(args(num_tokens=0)) == 0                    # nothing to do
+    # the MXFP8 shared input: shared_x_sf and shared_block_m exactly for fp8
+    fp8 = dict(shared_x=FAKE, shared_x_stride0=256, shared_x_dtype=B.MOE_SHARED_FP8)
+    assert run(args(**fp8)) == 1                           # no shared_x_sf
+    assert run(args(**fp8, shared_x_sf=FAKE, shared_x_sf_stride0=2, shared_x_sf_stride1=1,
+                    shared_x_sf_rows=128)) == 1            # no shared_block_m
+    assert run(args(shared_x=FAKE, shared_x_stride0=256, shared_x_sf=FAKE,
+                    shared_block_m=64, shared_x_sf_rows=128)) == 1  # bf16 shared_x with pages
+    assert run(args(**fp8, shared_x_sf=FAKE, shared_x_sf_stride0=2, shared_x_sf_stride1=1,
+                    shared_x_sf_rows=100, shared_block_m=64)) == 2  # needs 128 rows
+    assert run(args(**dict(fp8, shared_x_dtype=7))) == 1  # bad dtype
+    assert run(args(shared_x=FAKE, shared_x_stride0=256, shared_x_dtype=B.MOE_SHARED_FP8,
+                    shared_x_sf=FAKE + 0, shared_x_sf_stride0=2, shared_x_sf_stride1=1,
+                    shared_x_sf_rows=128, shared_block_m=64, hidden=FAKE + 8)) == 4

@@ -81,3 +81,67 @@ def test_reduce_gather_exact(cuda):
     torch.cuda.synchronize()
     exp = out_b[torch.from_numpy(ids[:, 0]), torch.from_numpy(slots[:, 0].astype(np.int64))]
     assert torch.equal(out.cpu(), exp)
+
+
+@pytest.mark.parametrize("contig", [False, True])
+def test_reduce_token_bound(cuda, orc, contig):
+    """num_valid_tokens (a device scalar): rows below it match the oracle's
+    bounded S8, rows at or past it keep their previous contents."""
+    T, k, E, M, K = 77, 8, 16, 64, 7168
+    rng = np.random.default_rng(91 + contig)
+    out_b = torch.from_numpy(rng.standard_normal((E, M, K), dtype=np.float32)).to(torch.bfloat16)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int64)
+    slots = rng.integers(-1, M, size=(T, k)).astype(np.int32)
+    if contig:
+        slots = np.where(slots >= 0, ids * M + slots, -1).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    dev = torch.device("cuda")
+    args = (out_b.to(dev), None if contig else torch.from_numpy(ids).to(dev),
+            torch.from_numpy(slots).to(dev), torch.from_numpy(w).to(dev))
+    ob = bf16_bits(out_b).reshape(E * M, K)
+    nv = torch.zeros(1, dtype=torch.int32, device=dev)
+    for bound in (0, 1, 13, T, 200, -5):
+        nv.fill_(bound)
+        out = torch.full((T, K), -1, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        B.moe_topk_reduce(*args, out, num_valid_tokens=nv)
+        torch.cuda.synchronize()
+        ref = orc.topk_reduce(ob, None if contig else ids, slots, w, M,
+                              num_valid=max(bound, 0), fill=0xFFFF)
+        got = bf16_bits(out)
+        n = min(max(bound, 0), T)
+        assert np.all(got[n:] == 0xFFFF), f"bound {bound}: rows past it were written"
+        rv = bf16_vals(ref[:n]).astype(np.float64)
+        gv = bf16_vals(got[:n]).astype(np.float64)
+        assert np.all(np.abs(gv - rv) <= np.abs(rv) * 2.0 ** -7 + 1e-3), f"bound {bound}"
+
+
+def test_reduce_token_bound_in_a_graph(cuda, orc):
+    """One reduce captured in a CUDA graph for the largest batch serves a
+    smaller one by updating the device scalar before each replay."""
+    T, k, E, M, K = 64, 4, 8, 32, 1024
+    rng = np.random.default_rng(5)
+    dev = torch.device("cuda")
+    out_b = torch.from_numpy(rng.standard_normal((E, M, K), dtype=np.float32)).to(
+        torch.bfloat16).to(dev)
+    ids = torch.from_numpy(rng.integers(0, E, size=(T, k)).astype(np.int64)).to(dev)
+    slots = torch.from_numpy(rng.integers(0, M, size=(T, k)).astype(np.int32)).to(dev)
+    w = torch.from_numpy(rng.random((T, k)).astype(np.float32)).to(dev)
+    out = torch.zeros((T, K), dtype=torch.bfloat16, device=dev)
+    nv = torch.full((1,), T, dtype=torch.int32, device=dev)
+    B.moe_topk_reduce(out_b, ids, slots, w, out, num_valid_tokens=nv)  # warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.moe_topk_reduce(out_b, ids, slots, w, out, num_valid_tokens=nv)
+    full = orc.topk_reduce(bf16_bits(out_b).reshape(E * M, K), ids.cpu().numpy(),
+                           slots.cpu().numpy(), w.cpu().numpy(), M)
+    for bound in (T, 10, 0, 33):
+        out.view(torch.int16).fill_(-1)
+        nv.fill_(bound)
+        g.replay()
+        torch.cuda.synchronize()
+        got = bf16_bits(out)
+        assert np.all(got[bound:] == 0xFFFF)
+        gv = bf16_vals(got[:bound]).astype(np.float64)
+        rv = bf16_vals(full[:bound]).astype(np.float64)
+        assert np.all(np.abs(gv - rv) <= np.abs(rv) * 2.0 ** -7 + 1e-3)

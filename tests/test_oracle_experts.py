@@ -164,6 +164,29 @@ def test_reduce_gather_and_convex(orc):
     del rng
 
 
+def test_reduce_token_bound(orc):
+    """moe_fused_mul_sum's num_valid_tokens: rows below the bound are the
+    unbounded reduce's, rows at or past it are not written; a bound at or past
+    T, or none, is the plain reduce; a bound of 0 writes nothing."""
+    T, K, M, E, k = 9, 128, 4, 3, 2
+    rng = np.random.default_rng(8)
+    ob = _bf16_bits(torch.from_numpy(rng.standard_normal((E * M, K), dtype=np.float32))
+                    .to(torch.bfloat16))
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int64)
+    slot = rng.integers(0, M, size=(T, k)).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    full = orc.topk_reduce(ob, ids, slot, w, M)
+    for bound in (0, 1, 5, T, T + 3):
+        got = orc.topk_reduce(ob, ids, slot, w, M, num_valid=bound, fill=0xFFFF)
+        n = min(bound, T)
+        assert np.array_equal(got[:n], full[:n])
+        assert np.all(got[n:] == 0xFFFF)
+    # the contiguous layout (rows in route_slot) obeys the same bound
+    rows = (ids * M + slot).astype(np.int32)
+    got = orc.topk_reduce(ob, None, rows, w, M, num_valid=4, fill=0xFFFF)
+    assert np.array_equal(got[:4], full[:4]) and np.all(got[4:] == 0xFFFF)
+
+
 # ------------------------------------------------------- brute force, tiny
 def _requant_closed_form(y):
     """Independent requant of one fp32 vector in 128-groups (torch cast)."""
