@@ -53,7 +53,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     if force:
         for f in os.listdir(BUILD_DIR):
-            os.remove(os.path.join(BUILD_DIR, f))
+            if os.path.isfile(os.path.join(BUILD_DIR, f)):
+                os.remove(os.path.join(BUILD_DIR, f))
     srcs = sources()
     with ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         results = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
