@@ -120,6 +120,90 @@ __device__ __forceinline__ int64_t repack_route(const StageParams& p, int64_t t,
   return id;
 }
 
+// The repack of routes r, r + stride, ... below R, four routes per thread at
+// a time: the padding flag, id and weight loads of the four are issued
+// together, then their replica counts, then their physical ids, so that each
+// dependent load of the EPLB map is paid once per four routes instead of once
+// per route.  Same results as repack_route on each route.
+template <typename IdT, typename WT>
+__device__ __forceinline__ void repack_strided(const StageParams& p, int64_t r, int64_t stride,
+                                               int64_t R, bool record_on, int64_t unpadded,
+                                               int* smem_load) {
+  constexpr int U = 4;
+  for (; r < R; r += stride * U) {
+    int64_t id[U], t[U], j[U];
+    float w[U];
+    bool act[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t ru = r + u * stride;
+      act[u] = ru < R;
+      t[u] = act[u] ? ru / p.top_k : 0;
+      j[u] = act[u] ? ru - t[u] * p.top_k : 0;
+      id[u] = -1;
+      w[u] = 0.0f;
+      if (act[u]) {
+        const bool is_pad = p.pad ? (p.pad[t[u] * p.ps0] != 0) : false;
+        id[u] = (int64_t)(reinterpret_cast<const IdT*>(p.ids)[t[u] * p.is0 + j[u] * p.is1]);
+        if constexpr (sizeof(WT) == 4) {
+          w[u] = reinterpret_cast<const float*>(p.wts)[t[u] * p.ws0 + j[u] * p.ws1];
+        } else {
+          w[u] = bf16_bits_to_f32(
+              reinterpret_cast<const uint16_t*>(p.wts)[t[u] * p.ws0 + j[u] * p.ws1]);
+        }
+        if (is_pad) {
+          id[u] = -1;
+          w[u] = 0.0f;
+        }
+      }
+    }
+    if (p.l2p != nullptr) {
+      int32_t reps[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        reps[u] = 0;
+        if (act[u] && id[u] >= 0) {
+          if (id[u] >= p.num_logical) {
+            set_status(p.status, MOE_DEV_BAD_EXPERT);
+            id[u] = -1;
+          } else {
+            reps[u] = p.rep_count[id[u]];
+          }
+        }
+      }
+      int64_t phys[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        phys[u] = -1;
+        if (act[u] && id[u] >= 0 && reps[u] >= 1)
+          phys[u] = p.l2p[id[u] * p.map_stride + (t[u] % reps[u])];
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (!(act[u] && id[u] >= 0)) continue;
+        if (reps[u] < 1 || phys[u] < 0 || (p.load != nullptr && phys[u] >= p.num_physical)) {
+          set_status(p.status, MOE_DEV_BAD_EXPERT);
+          id[u] = -1;
+        } else {
+          id[u] = phys[u];
+          if (p.load != nullptr && record_on && t[u] < unpadded) {
+            if (smem_load != nullptr)
+              atomicAdd(&smem_load[phys[u]], 1);
+            else
+              atomicAdd(&p.load[phys[u]], 1);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!act[u]) continue;
+      p.ids_out[t[u] * p.ios0 + j[u] * p.ios1] = id[u];
+      p.w_out[t[u] * p.wos0 + j[u] * p.wos1] = w[u];
+    }
+  }
+}
+
 __device__ __forceinline__ void record_flags(const StageParams& p, bool& record_on,
                                              int64_t& unpadded) {
   record_on = p.record != nullptr && (*p.record != 0);
@@ -413,8 +497,7 @@ __device__ __forceinline__ void repack_recorded(const StageParams& p, int64_t r0
                                                 int64_t unpadded, int* s_load) {
   for (int i = threadIdx.x; i < p.num_physical; i += blockDim.x) s_load[i] = 0;
   __syncthreads();
-  for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x)
-    repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, true, unpadded, s_load);
+  repack_strided<IdT, WT>(p, r0 + threadIdx.x, blockDim.x, r1, true, unpadded, s_load);
   __syncthreads();
   for (int i = threadIdx.x; i < p.num_physical; i += blockDim.x)
     if (s_load[i] != 0) atomicAdd(&p.load[i], s_load[i]);
@@ -479,9 +562,8 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
                                  s_load);
       }
     } else {
-      for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R;
-           r += (int64_t)gridDim.x * blockDim.x)
-        repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
+      repack_strided<IdT, WT>(p, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                              (int64_t)gridDim.x * blockDim.x, R, record_on, unpadded, nullptr);
     }
   }
 }
@@ -645,8 +727,6 @@ __device__ __forceinline__ float warp_max(float v) {
 template <typename IdT, typename WT, int NBL, bool SHARED_FP8>
 __global__ void __launch_bounds__(128) nvfp4_kernel(Nvfp4Params q, StageParams p) {
   const int lane = threadIdx.x & 31;
-  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   // RN(1 / dec(code)) for every E4M3 code of a non-negative scale (0x7F: NaN)
   __shared__ float s_rcp[128];
   for (int i = threadIdx.x; i < 128; i += blockDim.x) s_rcp[i] = __frcp_rn(e4m3_to_f32(i));
@@ -656,8 +736,29 @@ __global__ void __launch_bounds__(128) nvfp4_kernel(Nvfp4Params q, StageParams p
   if (blockIdx.x == 0 && q.l2_alpha != nullptr)
     for (int64_t e = threadIdx.x; e < q.n_local; e += blockDim.x)
       q.l2_alpha[e] = __fmul_rn(q.w2gs[e], q.l2s);
+  // routing: the same repack as the fp8 staging.  With load recording on and
+  // a large grid, a few blocks are set aside for it from the start, so that
+  // its dependent-load chains overlap the row streaming instead of trailing it.
+  __shared__ int s_load[kLoadBins];
+  bool record_on;
+  int64_t unpadded;
+  record_flags(p, record_on, unpadded);
+  const int64_t R = p.T * p.top_k;
+  const bool recorded = record_on && p.load != nullptr && p.num_physical <= kLoadBins;
+  const int64_t nrep = recorded ? min((int64_t)gridDim.x, (int64_t)kLoadBlocks) : 0;
+  const bool set_aside = recorded && gridDim.x >= 4 * kLoadBlocks;
+  if (set_aside && blockIdx.x < nrep) {
+    const int64_t per = (R + nrep - 1) / nrep;
+    repack_recorded<IdT, WT>(p, blockIdx.x * per, min(R, (blockIdx.x + 1) * per), unpadded,
+                             s_load);
+    return;
+  }
+  const int64_t sblock = set_aside ? blockIdx.x - nrep : blockIdx.x;
+  const int64_t sgrid = set_aside ? gridDim.x - nrep : gridDim.x;
+  const int64_t swarp = (sblock * blockDim.x + threadIdx.x) >> 5;
+  const int64_t snwarps = (sgrid * blockDim.x) >> 5;
   const int64_t nb = q.K / 16;  // a multiple of 8 (K % 128 == 0)
-  for (int64_t t = gwarp; t < q.T; t += nwarps) {
+  for (int64_t t = swarp; t < q.T; t += snwarps) {
     const uint16_t* row = q.hidden + t * q.hs0;
     if constexpr (NBL > 0) {
       uint4 va[NBL], vb[NBL];
@@ -706,23 +807,15 @@ __global__ void __launch_bounds__(128) nvfp4_kernel(Nvfp4Params q, StageParams p
       }
     }
   }
-  // routing: the same repack as the fp8 staging
-  bool record_on;
-  int64_t unpadded;
-  record_flags(p, record_on, unpadded);
-  const int64_t R = p.T * p.top_k;
-  if (record_on && p.load != nullptr && p.num_physical <= kLoadBins) {
-    __shared__ int s_load[kLoadBins];
-    const int64_t nrep = min((int64_t)gridDim.x, (int64_t)kLoadBlocks);
-    if (blockIdx.x < nrep) {
+  if (recorded) {
+    if (!set_aside && blockIdx.x < nrep) {
       const int64_t per = (R + nrep - 1) / nrep;
       repack_recorded<IdT, WT>(p, blockIdx.x * per, min(R, (blockIdx.x + 1) * per), unpadded,
                                s_load);
     }
   } else {
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < R;
-         r += (int64_t)gridDim.x * blockDim.x)
-      repack_route<IdT, WT>(p, r / p.top_k, r % p.top_k, record_on, unpadded);
+    repack_strided<IdT, WT>(p, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                            (int64_t)gridDim.x * blockDim.x, R, record_on, unpadded, nullptr);
   }
 }
 
