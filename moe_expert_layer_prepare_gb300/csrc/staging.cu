@@ -819,6 +819,165 @@ __global__ void __launch_bounds__(128) nvfp4_kernel(Nvfp4Params q, StageParams p
   }
 }
 
+// ---------------------------------------------------------------------------
+// NVFP4 token staging for rows of up to 8192 values, streamed through shared
+// memory.  One block per SM; each of its row warps owns a row buffer in
+// shared memory, fills it with a 1-D bulk copy (cp.async.bulk, completion
+// counted on the buffer's mbarrier) and quantises the landed row from shared
+// memory, then refills the buffer with its next row.  As many row warps as
+// row buffers fit in shared memory (up to RING_MAX_WARPS) keep that many rows
+// in flight per SM, bounded by shared memory rather than by registers.  The
+// last two warps do the top-k repack and EPLB map of the block's share of the
+// routes at the same time.  Same per-row arithmetic as nvfp4_kernel
+// (nvfp4_block, shared_fp8_block).  Measured on staging_stress with 4-14 row
+// warps and one to three buffers each: more row warps win (12 or more).
+// ---------------------------------------------------------------------------
+constexpr int RING_MAX_WARPS = 14;
+constexpr int RING_ROUTING_WARPS = 2;
+
+__device__ __forceinline__ void bulk_row_load(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool ring_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for a row copy (2 s of globaltimer); false on expiry.
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity) {
+  if (ring_try_wait(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t it = 1;; ++it) {
+    if (ring_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u) {
+      uint64_t t1;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+      if (t1 - t0 > 2000000000ull) return false;
+    }
+  }
+}
+
+template <typename IdT, typename WT, int NBL, bool SHARED_FP8>
+__global__ void __launch_bounds__((RING_MAX_WARPS + RING_ROUTING_WARPS) * 32, 1)
+    nvfp4_ring_kernel(Nvfp4Params q, StageParams p) {
+  extern __shared__ __align__(128) uint8_t ring_smem[];
+  __shared__ float s_rcp[128];
+  __shared__ __align__(8) uint64_t s_bar[RING_MAX_WARPS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row_warps = (int)(blockDim.x >> 5) - RING_ROUTING_WARPS;
+  const uint32_t rowbytes = (uint32_t)(q.K * 2);
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) s_rcp[i] = __frcp_rn(e4m3_to_f32(i));
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < row_warps; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(
+                       (uint32_t)__cvta_generic_to_shared(&s_bar[i]))
+                   : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+  if (blockIdx.x == 0 && q.l2_alpha != nullptr)
+    for (int64_t e = threadIdx.x; e < q.n_local; e += blockDim.x)
+      q.l2_alpha[e] = __fmul_rn(q.w2gs[e], q.l2s);
+  bool record_on;
+  int64_t unpadded;
+  record_flags(p, record_on, unpadded);
+
+  if (warp >= row_warps) {
+    // ---------------------------------------------------------- routing
+    const int rt = threadIdx.x - row_warps * 32;  // 0..63
+    const int64_t R = p.T * p.top_k;
+    const bool recorded = record_on && p.load != nullptr && p.num_physical <= kLoadBins;
+    if (recorded) {
+      // this block's contiguous share of the routes, counted in a shared
+      // histogram (after the ring buffers) and added once per non-zero bin
+      int* s_load = reinterpret_cast<int*>(ring_smem + row_warps * rowbytes);
+      for (int i = rt; i < p.num_physical; i += 64) s_load[i] = 0;
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      const int64_t per = (R + gridDim.x - 1) / gridDim.x;
+      const int64_t r0 = (int64_t)blockIdx.x * per, r1 = min(R, r0 + per);
+      repack_strided<IdT, WT>(p, r0 + rt, 64, r1, true, unpadded, s_load);
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      for (int i = rt; i < p.num_physical; i += 64)
+        if (s_load[i] != 0) atomicAdd(&p.load[i], s_load[i]);
+    } else {
+      repack_strided<IdT, WT>(p, (int64_t)blockIdx.x * 64 + rt, (int64_t)gridDim.x * 64, R,
+                              record_on, unpadded, nullptr);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------- rows
+  const int64_t stride = (int64_t)gridDim.x * row_warps;
+  const int64_t t0 = (int64_t)blockIdx.x * row_warps + warp;
+  const uint8_t* row = ring_smem + warp * rowbytes;
+  const uint32_t row_s = (uint32_t)__cvta_generic_to_shared(row);
+  const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar[warp]);
+  const int64_t nb = q.K / 16;
+  if (t0 < q.T && lane == 0) bulk_row_load(row_s, q.hidden + t0 * q.hs0, rowbytes, bar);
+  __syncwarp();
+  uint32_t parity = 0;
+  for (int64_t t = t0; t < q.T; t += stride) {
+    if (!__all_sync(0xFFFFFFFFu, ring_wait(bar, parity))) {
+      // a copy that has not landed in 2 s: report it, give it one more
+      // bounded wait so that it is not in flight when the block exits, and
+      // stop using the buffer
+      set_status(p.status, MOE_DEV_TIMEOUT);
+      ring_wait(bar, parity);
+      break;
+    }
+    parity ^= 1u;
+    uint32_t bm[NBL];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int k = 0; k < NBL; ++k) {
+      const int64_t b = lane + 32 * k;
+      bm[k] = 0;
+      if (b < nb) {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + b * 32);
+        const uint4 c = *reinterpret_cast<const uint4*>(row + b * 32 + 16);
+        bm[k] = block_absmax2(a, c);
+        m2 = absmax_bf16x2(m2, bm[k]);
+      }
+    }
+    const float amax = warp_max(absmax2_to_f32(m2));
+    const float xs = __fdiv_rn(amax, 2688.0f);
+    if (lane == 0) q.x_scales[t] = xs;
+    const float inv = amax > 0.0f ? __frcp_rn(xs) : 0.0f;
+#pragma unroll
+    for (int k = 0; k < NBL; ++k) {
+      const int64_t b = lane + 32 * k;
+      const bool act = b < nb;
+      const uint4 a = act ? *reinterpret_cast<const uint4*>(row + b * 32) : make_uint4(0, 0, 0, 0);
+      const uint4 c =
+          act ? *reinterpret_cast<const uint4*>(row + b * 32 + 16) : make_uint4(0, 0, 0, 0);
+      nvfp4_block(q, s_rcp, t, b, act, a, c, bm[k], inv);
+      if constexpr (SHARED_FP8) shared_fp8_block(q, t, b, act, a, c, bm[k]);
+    }
+    // the buffer is read: refill it with this warp's next row
+    __syncwarp();
+    if (t + stride < q.T) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (lane == 0) bulk_row_load(row_s, q.hidden + (t + stride) * q.hs0, rowbytes, bar);
+      __syncwarp();
+    }
+  }
+}
+
 }  // namespace moe
 
 // ---------------------------------------------------------------------------
@@ -985,6 +1144,35 @@ static moe_status_t launch_nvfp4_typed(const moe::Nvfp4Params& q, const StagePar
            : nbl <= 16 ? moe::nvfp4_kernel<IdT, WT, 16, F>
                        : moe::nvfp4_kernel<IdT, WT, 0, F>;
   };
+  if (nbl <= 16) {
+    // rows of up to 8192 values: streamed through shared memory, one block
+    // of row warps and two routing warps per SM
+    auto pick_ring = [&](auto fp8) {
+      constexpr bool F = decltype(fp8)::value;
+      return nbl <= 4    ? moe::nvfp4_ring_kernel<IdT, WT, 4, F>
+             : nbl <= 8  ? moe::nvfp4_ring_kernel<IdT, WT, 8, F>
+             : nbl <= 14 ? moe::nvfp4_ring_kernel<IdT, WT, 14, F>
+                         : moe::nvfp4_ring_kernel<IdT, WT, 16, F>;
+    };
+    auto k = q.shared_q != nullptr ? pick_ring(std::true_type{}) : pick_ring(std::false_type{});
+    // as many row buffers as fit next to the load histogram (and the static
+    // 640 bytes) in 227 KB of shared memory
+    const size_t rowbytes = (size_t)(q.K * 2);
+    const size_t hist = (size_t)moe::kLoadBins * sizeof(int);
+    int row_warps = (int)((227 * 1024 - 1024 - hist) / rowbytes);
+    if (row_warps > moe::RING_MAX_WARPS) row_warps = moe::RING_MAX_WARPS;
+    const size_t smem = (size_t)row_warps * rowbytes + hist;
+    cudaError_t ae = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (ae != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "nvfp4 smem attribute: %s", cudaGetErrorString(ae));
+    int64_t blocks = (q.T + row_warps - 1) / row_warps;
+    if (blocks > num_sms()) blocks = num_sms();
+    if (blocks < 1) blocks = 1;
+    cudaError_t e = launch_pdl(k, dim3((unsigned)blocks),
+                               dim3((row_warps + moe::RING_ROUTING_WARPS) * 32), smem, s, q, p);
+    if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "nvfp4 launch: %s", cudaGetErrorString(e));
+    return MOE_OK;
+  }
   auto k = q.shared_q != nullptr ? pick(std::true_type{}) : pick(std::false_type{});
   int64_t blocks = (q.T + 3) / 4;
   if (blocks < 1) blocks = 1;
