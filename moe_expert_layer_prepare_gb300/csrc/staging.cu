@@ -978,6 +978,98 @@ __global__ void __launch_bounds__((RING_MAX_WARPS + RING_ROUTING_WARPS) * 32, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// The fp8 (1x128) staging of long batches, streamed through shared memory the
+// same way as nvfp4_ring_kernel: one block per SM, each row warp fills its
+// row buffer with a bulk copy and quantises the landed row task by task
+// (quant_task: the same per-task arithmetic, stores, shared pages and
+// dispatch scatter as quant_kernel).  With the repack folded in, the last two
+// warps repack the block's share of the routes meanwhile.
+// ---------------------------------------------------------------------------
+template <int SF_MODE, bool REPACK, bool DISPATCH, typename IdT, typename WT, bool SHARED>
+__global__ void __launch_bounds__((RING_MAX_WARPS + RING_ROUTING_WARPS) * 32, 1)
+    quant_ring_kernel(StageParams p) {
+  extern __shared__ __align__(128) uint8_t ring_smem[];
+  __shared__ __align__(8) uint64_t s_bar[RING_MAX_WARPS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row_warps = (int)(blockDim.x >> 5) - RING_ROUTING_WARPS;
+  const uint32_t rowbytes = (uint32_t)(p.K * 2);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < row_warps; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(
+                       (uint32_t)__cvta_generic_to_shared(&s_bar[i]))
+                   : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp >= row_warps) {
+    // ---------------------------------------------------------- routing
+    if constexpr (REPACK) {
+      bool record_on;
+      int64_t unpadded;
+      record_flags(p, record_on, unpadded);
+      const int rt = threadIdx.x - row_warps * 32;  // 0..63
+      const int64_t R = p.T * p.top_k;
+      if (record_on && p.load != nullptr && p.num_physical <= kLoadBins) {
+        int* s_load = reinterpret_cast<int*>(ring_smem + row_warps * rowbytes);
+        for (int i = rt; i < p.num_physical; i += 64) s_load[i] = 0;
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        const int64_t per = (R + gridDim.x - 1) / gridDim.x;
+        const int64_t r0 = (int64_t)blockIdx.x * per, r1 = min(R, r0 + per);
+        repack_strided<IdT, WT>(p, r0 + rt, 64, r1, true, unpadded, s_load);
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        for (int i = rt; i < p.num_physical; i += 64)
+          if (s_load[i] != 0) atomicAdd(&p.load[i], s_load[i]);
+      } else {
+        repack_strided<IdT, WT>(p, (int64_t)blockIdx.x * 64 + rt, (int64_t)gridDim.x * 64, R,
+                                record_on, unpadded, nullptr);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------- rows
+  const int64_t stride = (int64_t)gridDim.x * row_warps;
+  const int64_t t0 = (int64_t)blockIdx.x * row_warps + warp;
+  const uint8_t* row = ring_smem + warp * rowbytes;
+  const uint32_t row_s = (uint32_t)__cvta_generic_to_shared(row);
+  const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar[warp]);
+  const int half = lane >> 4;
+  if (t0 < p.T && lane == 0) bulk_row_load(row_s, p.hidden + t0 * p.hs0, rowbytes, bar);
+  __syncwarp();
+  uint32_t parity = 0;
+  for (int64_t t = t0; t < p.T; t += stride) {
+    if (!__all_sync(0xFFFFFFFFu, ring_wait(bar, parity))) {
+      // a copy that has not landed in 2 s: report it, give it one more
+      // bounded wait so that it is not in flight when the block exits, and
+      // stop using the buffer
+      set_status(p.status, MOE_DEV_TIMEOUT);
+      ring_wait(bar, parity);
+      break;
+    }
+    parity ^= 1u;
+    for (int64_t w = 0; w < p.W; ++w) {
+      // task w: groups 4w..4w+3, lane's 16 bytes of each half (see quant_kernel)
+      const uint8_t* src = row + (4 * w * kGroup + lane * 8) * 2;
+      const uint4 vA = (4 * w + half < p.G) ? *reinterpret_cast<const uint4*>(src)
+                                            : make_uint4(0, 0, 0, 0);
+      const uint4 vB = (4 * w + 2 + half < p.G) ? *reinterpret_cast<const uint4*>(src + 512)
+                                                : make_uint4(0, 0, 0, 0);
+      quant_task<SF_MODE, DISPATCH, SHARED>(p, t, w, vA, vB, lane);
+    }
+    // the buffer is read: refill it with this warp's next row
+    __syncwarp();
+    if (t + stride < p.T) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (lane == 0) bulk_row_load(row_s, p.hidden + (t + stride) * p.hs0, rowbytes, bar);
+      __syncwarp();
+    }
+  }
+}
+
 }  // namespace moe
 
 // ---------------------------------------------------------------------------
@@ -1005,10 +1097,34 @@ static int64_t quant_grid(Kernel k, int64_t tasks) {
   return blocks < 1 ? 1 : blocks;
 }
 
+// Long batches of rows up to 8192 values stream through shared memory
+// (quant_ring_kernel); short ones spread each row over many warps
+// (quant_kernel), which keeps a decode step's few rows from serialising.
+constexpr int64_t kRingMinTokens = 1024;
+
+static bool use_ring(const StageParams& p) { return p.K <= 8192 && p.T >= kRingMinTokens; }
+
+template <typename Kernel>
+static cudaError_t launch_ring(Kernel k, const StageParams& p, cudaStream_t s) {
+  const size_t rowbytes = (size_t)(p.K * 2);
+  const size_t hist = (size_t)moe::kLoadBins * sizeof(int);
+  int row_warps = (int)((227 * 1024 - 1024 - hist) / rowbytes);
+  if (row_warps > moe::RING_MAX_WARPS) row_warps = moe::RING_MAX_WARPS;
+  const size_t smem = (size_t)row_warps * rowbytes + hist;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int64_t blocks = (p.T + row_warps - 1) / row_warps;
+  if (blocks > num_sms()) blocks = num_sms();
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(k, dim3((unsigned)blocks), dim3((row_warps + moe::RING_ROUTING_WARPS) * 32),
+                    smem, s, p);
+}
+
 template <typename IdT, typename WT>
 static moe_status_t launch_typed(StageParams& p, bool dispatch, int sf_mode, cudaStream_t s) {
   const int64_t tasks = p.T * p.W;
   const int threads = 256;
+  const bool ring = use_ring(p);
   if (dispatch) {
     const int64_t R = p.T * p.top_k;
     const int64_t B = (R + 1023) / 1024;
@@ -1028,31 +1144,56 @@ static moe_status_t launch_typed(StageParams& p, bool dispatch, int sf_mode, cud
       return set_error(MOE_ERR_CUDA, "route_kernel launch: %s", cudaGetErrorString(le));
     // the shared-expert pages are a separate instantiation: even untaken,
     // their code costs the streaming loop ~10%
-    auto qk = sf_mode == MOE_SF_FP32
-                  ? moe::quant_kernel<MOE_SF_FP32, false, true, IdT, WT, false>
-                  : (p.shared_sf != nullptr
-                         ? moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, true>
-                         : moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, false>);
-    le = launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+    if (ring) {
+      auto qk = sf_mode == MOE_SF_FP32
+                    ? moe::quant_ring_kernel<MOE_SF_FP32, false, true, IdT, WT, false>
+                    : (p.shared_sf != nullptr
+                           ? moe::quant_ring_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, true>
+                           : moe::quant_ring_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT,
+                                                    false>);
+      le = launch_ring(qk, p, s);
+    } else {
+      auto qk = sf_mode == MOE_SF_FP32
+                    ? moe::quant_kernel<MOE_SF_FP32, false, true, IdT, WT, false>
+                    : (p.shared_sf != nullptr
+                           ? moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, true>
+                           : moe::quant_kernel<MOE_SF_UE8M0_PACKED, false, true, IdT, WT, false>);
+      le = launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+    }
     if (le != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "quant_kernel launch: %s", cudaGetErrorString(le));
   } else {
     switch (sf_mode) {
       case MOE_SF_NONE: {
-        auto qk = moe::quant_kernel<MOE_SF_NONE, true, false, IdT, WT, false>;
-        launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+        if (ring) {
+          launch_ring(moe::quant_ring_kernel<MOE_SF_NONE, true, false, IdT, WT, false>, p, s);
+        } else {
+          auto qk = moe::quant_kernel<MOE_SF_NONE, true, false, IdT, WT, false>;
+          launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+        }
         break;
       }
       case MOE_SF_UE8M0_PACKED: {
-        auto qk = p.shared_sf != nullptr
-                      ? moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT, true>
-                      : moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT, false>;
-        launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+        if (ring) {
+          auto qk = p.shared_sf != nullptr
+                        ? moe::quant_ring_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT, true>
+                        : moe::quant_ring_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT, false>;
+          launch_ring(qk, p, s);
+        } else {
+          auto qk = p.shared_sf != nullptr
+                        ? moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT, true>
+                        : moe::quant_kernel<MOE_SF_UE8M0_PACKED, true, false, IdT, WT, false>;
+          launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+        }
         break;
       }
       default: {
-        auto qk = moe::quant_kernel<MOE_SF_FP32, true, false, IdT, WT, false>;
-        launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+        if (ring) {
+          launch_ring(moe::quant_ring_kernel<MOE_SF_FP32, true, false, IdT, WT, false>, p, s);
+        } else {
+          auto qk = moe::quant_kernel<MOE_SF_FP32, true, false, IdT, WT, false>;
+          launch_pdl(qk, dim3((unsigned)quant_grid(qk, tasks)), dim3(threads), 0, s, p);
+        }
         break;
       }
     }

@@ -52,6 +52,12 @@ CASES = [
     (200, 7168, 8, torch.int32, torch.float32, True, B.MOE_SF_UE8M0_PACKED),
     (33, 1024, 4, torch.int32, torch.float32, True, B.MOE_SF_FP32),
     (16, 384, 1, torch.int32, torch.float32, False, B.MOE_SF_NONE),
+    # from 1024 tokens the rows stream through shared memory (one row buffer
+    # per warp): every sf mode, both id and weight dtypes, a ragged last word
+    (1500, 1152, 4, torch.int32, torch.float32, True, B.MOE_SF_UE8M0_PACKED),
+    (1100, 640, 3, torch.int64, torch.bfloat16, False, B.MOE_SF_FP32),
+    (1030, 384, 1, torch.int32, torch.float32, True, B.MOE_SF_NONE),
+    (2048, 8192, 2, torch.int32, torch.float32, False, B.MOE_SF_UE8M0_PACKED),
 ]
 
 
@@ -244,6 +250,7 @@ def _shared_pages(hidden, ids, w, block_m, dispatch=None, fill=0xEE, extra_rows=
     (257, 256, 128),    # whole pages plus one token
     (1000, 7168, 256),  # DeepSeek-V3 hidden size
     (64, 4096, 64),     # block smaller than a page
+    (3000, 7168, 512),  # a long batch: rows streamed through shared memory
 ])
 def test_shared_scale_pages(cuda, orc, T, K, block_m):
     """Shared-expert scale pages: every token's exponent bytes at its page
