@@ -279,11 +279,6 @@ __device__ __forceinline__ void tmem_wait_ld() {
                :                                                                                \
                : "memory")
 
-// dst[i] += r[i] * s for 32 columns (fp32, round to nearest).
-#define FMA32(dst, r, s)                                        \
-  _Pragma("unroll") for (int i_ = 0; i_ < 32; ++i_) (dst)[i_] = \
-      fmaf(__uint_as_float((r)[i_]), (s), (dst)[i_])
-
 // dst[i] += r[i] * s for 32 columns with packed fp32x2 FMAs (round to nearest).
 #define FMA32X2(dst, r, s)                                                            \
   _Pragma("unroll") for (int i_ = 0; i_ < 32; i_ += 2) {                              \
@@ -294,16 +289,10 @@ __device__ __forceinline__ void tmem_wait_ld() {
     (dst)[i_ + 1] = d_.y;                                                             \
   }
 
-// The epilogue's per-slab fold: plain FMAs in W13, packed pairs in W2
-// (measured: w2 ~4% faster with packed pairs, w13 unchanged).
-#define FOLD32(dst, r, s)        \
-  {                              \
-    if constexpr (W13) {         \
-      FMA32(dst, r, s);          \
-    } else {                     \
-      FMA32X2(dst, r, s);        \
-    }                            \
-  }
+// The epilogue's per-slab fold, in packed fp32x2 FMAs (measured against
+// single FMAs on prefill: w13 -1.7%, w2 -4%).
+#define FOLD32(dst, r, s) \
+  { FMA32X2(dst, r, s); }
 
 // ------------------------------------------------------------------ schedule
 struct Unit {
