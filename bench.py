@@ -457,7 +457,10 @@ def bench_experts(name, args, world, dev, peaks, flush, want_cpu):
                config=config_of(name, wl, args.layout, "fp8", world), roofline=roof,
                stages_ms=dict(prepare=round(med[0], 4), w13=round(med[1], 4),
                               w2=round(med[2], 4), reduce=round(med[3], 4),
-                              note="separate pass, events between the calls"),
+                              note="separate pass, events between the calls",
+                              # what staging + reduce add to the chained step:
+                              # the whole step less the two GEMMs' own times
+                              prepare_reduce_in_step=round(ms - med[1] - med[2], 4)),
                stages_gbs=dict(prepare=round(alg["stage_bytes"] / med[0] / 1e6, 1),
                                w13=round(w13_gbs, 1),
                                w2=round(alg["w2_bytes"] / med[2] / 1e6, 1),
@@ -529,7 +532,7 @@ def bench_staging(args, world, dev, peaks, flush, want_cpu, fmt):
     ms = max_over_ranks(world, median(t))
     nbytes = staging_bytes(T, K, k, wl, nvfp4)
     gbs = world * nbytes / (ms * 1e-3) / 1e9
-    kern = "nvfp4_kernel" if nvfp4 else "quant_kernel<UE8M0,repack>"
+    kern = "nvfp4_ring_kernel" if nvfp4 else "quant_ring_kernel<UE8M0,repack>"
     out = dict(value=round(gbs, 1), unit="GB/s", ms_per_step=round(ms, 4),
                dtype="bf16->e2m1 (e4m3/16, fp32/token)" if nvfp4 else
                "bf16->fp8e4m3 (fp32 scale math)",

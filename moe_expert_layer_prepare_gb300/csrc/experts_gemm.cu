@@ -55,13 +55,20 @@ constexpr int NUM_THREADS = 384;              // 12 warps = 3 warpgroups
 constexpr int EPI_WARP0 = 4;                  // warpgroups 1-2 are the epilogue
 constexpr int EPI_WARPS = 8;
 // Register split (setmaxnreg): the kernel is compiled for 168 registers per
-// thread (384 x 168 = 64512); warpgroup 0 (TMA, MMA, two idle warps) drops to
-// 40 and the two epilogue warpgroups rise to 232: 128 x 40 + 256 x 232 = 64512.
+// thread (384 x 168 = 64512); warpgroup 0 (TMA, MMA, the two scale-staging
+// warps) drops and the two epilogue warpgroups rise.  The split is chosen per
+// instantiation by what ptxas spills and what the GEMM then measures: the w2
+// GEMM compiles spill-free at 56 / 224, the w13 GEMM spills least at 72 / 216
+// (its fp32-scale form at 40 / 232).  Each sums to 128 x P + 256 x E <= 64512.
 constexpr int LAUNCH_REGS = 168;
-constexpr int PRODUCER_REGS = 40;
-constexpr int EPILOGUE_REGS = 232;
-static_assert(128 * PRODUCER_REGS + 256 * EPILOGUE_REGS <= NUM_THREADS * LAUNCH_REGS,
-              "register split exceeds the launch allocation");
+constexpr int producer_regs(bool w13, bool af32) { return !w13 ? 56 : (af32 ? 40 : 72); }
+constexpr int epilogue_regs(bool w13, bool af32) { return !w13 ? 224 : (af32 ? 232 : 216); }
+static_assert(128 * producer_regs(false, false) + 256 * epilogue_regs(false, false) <=
+                  NUM_THREADS * LAUNCH_REGS, "register split exceeds the launch allocation");
+static_assert(128 * producer_regs(true, false) + 256 * epilogue_regs(true, false) <=
+                  NUM_THREADS * LAUNCH_REGS, "register split exceeds the launch allocation");
+static_assert(128 * producer_regs(true, true) + 256 * epilogue_regs(true, true) <=
+                  NUM_THREADS * LAUNCH_REGS, "register split exceeds the launch allocation");
 constexpr int MAX_EXPERTS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 // Scale staging (UE8M0 activation scales): the two spare warps of warpgroup 0
@@ -452,7 +459,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int total_units = prefix[p.E] * p.n_tiles * p.splits;
 
   if (warp < EPI_WARP0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PRODUCER_REGS));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(producer_regs(W13, AF32)));
     // The producer and MMA loops run on all 32 lanes of their warp with
     // warp-uniform control flow, so every tcgen05 / TMA operand stays
     // warp-uniform; one elected lane issues each instruction.
@@ -616,7 +623,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPILOGUE_REGS));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(epilogue_regs(W13, AF32)));
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                    // TMEM lane quarter
     const int h = (warp - EPI_WARP0) >> 2;     // column half

@@ -72,8 +72,9 @@ struct StageParams {
 };
 
 // Repack one route (t, j): int64 id (-1 for padding), fp32 weight, EPLB map and
-// load record.  Returns the id written.
-template <typename IdT, typename WT>
+// load record.  Returns the id written.  With WRITE false only the id is
+// worked out: nothing is stored, counted or flagged.
+template <typename IdT, typename WT, bool WRITE = true>
 __device__ __forceinline__ int64_t repack_route(const StageParams& p, int64_t t, int64_t j,
                                                 bool record_on, int64_t unpadded,
                                                 int* smem_load = nullptr) {
@@ -91,21 +92,21 @@ __device__ __forceinline__ int64_t repack_route(const StageParams& p, int64_t t,
   }
   if (p.l2p != nullptr && id >= 0) {
     if (id >= p.num_logical) {
-      set_status(p.status, MOE_DEV_BAD_EXPERT);
+      if (WRITE) set_status(p.status, MOE_DEV_BAD_EXPERT);
       id = -1;
     } else {
       int32_t reps = p.rep_count[id];
       if (reps < 1) {
-        set_status(p.status, MOE_DEV_BAD_EXPERT);
+        if (WRITE) set_status(p.status, MOE_DEV_BAD_EXPERT);
         id = -1;
       } else {
         int64_t phys = p.l2p[id * p.map_stride + (t % reps)];
         if (phys < 0 || (p.load != nullptr && phys >= p.num_physical)) {
-          set_status(p.status, MOE_DEV_BAD_EXPERT);
+          if (WRITE) set_status(p.status, MOE_DEV_BAD_EXPERT);
           id = -1;
         } else {
           id = phys;
-          if (p.load != nullptr && record_on && t < unpadded) {
+          if (WRITE && p.load != nullptr && record_on && t < unpadded) {
             if (smem_load != nullptr)
               atomicAdd(&smem_load[phys], 1);
             else
@@ -115,8 +116,10 @@ __device__ __forceinline__ int64_t repack_route(const StageParams& p, int64_t t,
       }
     }
   }
-  p.ids_out[t * p.ios0 + j * p.ios1] = id;
-  p.w_out[t * p.wos0 + j * p.wos1] = w;
+  if constexpr (WRITE) {
+    p.ids_out[t * p.ios0 + j * p.ios1] = id;
+    p.w_out[t * p.wos0 + j * p.wos1] = w;
+  }
   return id;
 }
 
@@ -364,10 +367,12 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
   asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
-// One task after its two loads have landed.
-template <int SF_MODE, bool DISPATCH, bool SHARED>
+// One task after its two loads have landed.  With SMALL the destination row
+// of every route comes ready-made from srows (-1: not dispatched) and
+// route_slot is written elsewhere.
+template <int SF_MODE, bool DISPATCH, bool SHARED, bool SMALL = false>
 __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int64_t w, uint4 vA,
-                                           uint4 vB, int lane) {
+                                           uint4 vB, int lane, const int32_t* srows = nullptr) {
   const int half = lane >> 4;
   const int64_t gA = 4 * w + half, gB = 4 * w + 2 + half;
   const bool actA = gA < p.G, actB = gB < p.G;
@@ -418,7 +423,9 @@ __device__ __forceinline__ void quant_task(const StageParams& p, int64_t t, int6
       // Lane j works out route j's destination row (three dependent loads),
       // so the top_k chains run side by side; the rows are then broadcast.
       int64_t my_slot = -1, my_row = -1;
-      if (lane < p.top_k) {
+      if (SMALL && lane < p.top_k) {
+        my_row = srows[t * p.top_k + lane];
+      } else if (!SMALL && lane < p.top_k) {
         const int64_t r = t * p.top_k + lane;
         const int64_t e = p.ids_out[t * p.ios0 + lane * p.ios1];
         if (e >= 0 && e < p.E) {
@@ -488,6 +495,29 @@ __device__ __forceinline__ void load_batch(const StageParams& p, TaskBatch& b, u
   }
 }
 
+// The task loop of one warp: tasks base, base + nw, ... below `tasks`, with
+// the first batch (cur) already loaded; each batch's successor is loaded
+// before the batch is quantised.
+template <int SF_MODE, bool DISPATCH, bool SHARED, bool SMALL>
+__device__ __forceinline__ void quant_loop(const StageParams& p, TaskBatch& cur, uint32_t base,
+                                           uint32_t nw, uint32_t tasks, int lane,
+                                           const int32_t* srows) {
+  const uint32_t Wd = (uint32_t)p.W;
+  const uint32_t step = QUANT_BATCH * nw;
+  TaskBatch nxt;
+  for (; base < tasks; base += step) {
+    const bool more = base + step < tasks;
+    if (more) load_batch(p, nxt, base + step, nw, tasks, Wd, lane);
+#pragma unroll
+    for (int i = 0; i < QUANT_BATCH; ++i) {
+      if (base + i * nw < tasks)
+        quant_task<SF_MODE, DISPATCH, SHARED, SMALL>(p, cur.t[i], cur.w[i], cur.vA[i],
+                                                     cur.vB[i], lane, srows);
+    }
+    if (more) cur = nxt;
+  }
+}
+
 // Repack of routes [r0, r1) with the EPLB load counted in a shared-memory
 // histogram that is added to the global counters once per non-zero bin.
 // Per-route global atomics would land on the few L2 lines that hold the
@@ -521,7 +551,7 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
   const bool recorded = REPACK && record_on && p.load != nullptr && p.num_physical <= kLoadBins;
   const int64_t nrep = recorded ? min((int64_t)gridDim.x, (int64_t)kLoadBlocks) : 0;
   const bool set_aside = recorded && gridDim.x >= 4 * kLoadBlocks;
-  if (set_aside && blockIdx.x < nrep) {
+  if (REPACK && set_aside && blockIdx.x < nrep) {
     const int64_t per = (R + nrep - 1) / nrep;
     repack_recorded<IdT, WT>(p, blockIdx.x * per, min(R, (blockIdx.x + 1) * per), unpadded,
                              s_load);
@@ -534,22 +564,11 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
 
   // tasks index (token, word) pairs; the host guarantees T * W < 2^31
   const uint32_t tasks = (uint32_t)(p.T * p.W);
-  const uint32_t Wd = (uint32_t)p.W;
-  const uint32_t nw = (uint32_t)nwarps;
-  const uint32_t step = QUANT_BATCH * nw;
-  uint32_t base = (uint32_t)gwarp;
-  TaskBatch cur, nxt;
-  if (base < tasks) load_batch(p, cur, base, nw, tasks, Wd, lane);
-  for (; base < tasks; base += step) {
-    const bool more = base + step < tasks;
-    if (more) load_batch(p, nxt, base + step, nw, tasks, Wd, lane);
-#pragma unroll
-    for (int i = 0; i < QUANT_BATCH; ++i) {
-      if (base + i * nw < tasks)
-        quant_task<SF_MODE, DISPATCH, SHARED>(p, cur.t[i], cur.w[i], cur.vA[i], cur.vB[i], lane);
-    }
-    if (more) cur = nxt;
-  }
+  TaskBatch cur;
+  if ((uint32_t)gwarp < tasks) load_batch(p, cur, (uint32_t)gwarp, (uint32_t)nwarps, tasks,
+                                          (uint32_t)p.W, lane);
+  quant_loop<SF_MODE, DISPATCH, SHARED, false>(p, cur, (uint32_t)gwarp, (uint32_t)nwarps, tasks,
+                                               lane, nullptr);
 
   // Without recording (or on a small grid) the top-k repack (dependent
   // loads, no bandwidth) goes last so that its latency overlaps the other
@@ -568,6 +587,146 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// small_dispatch_kernel: the staging and dispatch of a batch of at most
+// kSmallRoutes routes in one launch, with no workspace and no host memset.
+// Every block maps all routes to their physical expert and ranks them in
+// route order (at most four 256-route passes over shared memory), so that no
+// block waits for another; block 0 alone stores the repacked ids and weights,
+// the EPLB load record, route_slot and the per-expert counts (and the
+// contiguous layout's first rows).  The first batch of hidden-state loads is
+// issued before the routing, so the two overlap; the blocks then quantise
+// their tasks and store each into its routed rows as quant_kernel does.
+// Dynamic smem: E ints (running counts, then first rows) + 8 * E uint16
+// (per-warp counts of one pass).
+// ---------------------------------------------------------------------------
+constexpr int kSmallRoutes = 1024;
+
+template <int SF_MODE, typename IdT, typename WT, bool SHARED>
+__global__ void __launch_bounds__(256) small_dispatch_kernel(StageParams p) {
+  extern __shared__ int32_t s_dyn[];
+  __shared__ int32_t s_row[kSmallRoutes];  // rank, then destination row (-1: none)
+  __shared__ int16_t s_e[kSmallRoutes];    // physical expert (-1: unrouted)
+  __shared__ int32_t s_wsum[8];
+  const int E = (int)p.E;
+  int32_t* s_run = s_dyn;
+  uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_dyn + E);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = (int)(p.T * p.top_k);
+  const bool lead = blockIdx.x == 0;
+  for (int i = tid; i < 5 * E; i += 256) s_dyn[i] = 0;  // E + 8E/2 words
+  pdl_wait();
+
+  // the first batch of this warp's tasks is in flight during the routing
+  const uint32_t tasks = (uint32_t)(p.T * p.W);
+  const uint32_t gwarp = (uint32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const uint32_t nwarps = (uint32_t)((gridDim.x * blockDim.x) >> 5);
+  TaskBatch cur;
+  if (gwarp < tasks) load_batch(p, cur, gwarp, nwarps, tasks, (uint32_t)p.W, lane);
+
+  bool record_on;
+  int64_t unpadded;
+  record_flags(p, record_on, unpadded);
+  for (int r = tid; r < R; r += 256) {
+    const int64_t t = r / p.top_k, j = r - t * p.top_k;
+    int64_t id = lead ? repack_route<IdT, WT, true>(p, t, j, record_on, unpadded)
+                      : repack_route<IdT, WT, false>(p, t, j, record_on, unpadded);
+    if (id >= E) {
+      if (lead) set_status(p.status, MOE_DEV_BAD_EXPERT);
+      id = -1;
+    }
+    s_e[r] = (int16_t)id;
+  }
+  __syncthreads();
+
+  // Stable rank of each route among the routes to its expert: 256 routes per
+  // pass in route order; within a pass, warps in order and lanes in order.
+  for (int c = 0; c < R; c += 256) {
+    const int r = c + tid;
+    const int e = r < R ? s_e[r] : -1;
+    const uint32_t same = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank_in_warp = __popc(same & lanemask_lt());
+    if (e >= 0 && rank_in_warp == 0) s_cnt[warp * E + e] = (uint16_t)__popc(same);
+    __syncthreads();
+    if (e >= 0) {
+      int base = s_run[e];
+      for (int w = 0; w < warp; ++w) base += s_cnt[w * E + e];
+      s_row[r] = base + rank_in_warp;
+    }
+    __syncthreads();
+    for (int ex = tid; ex < E; ex += 256) {
+      int tot = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        tot += s_cnt[w * E + ex];
+        s_cnt[w * E + ex] = 0;
+      }
+      s_run[ex] += tot;
+    }
+    __syncthreads();
+  }
+
+  // s_run[e] = routes to expert e.  Ranks become destination rows.
+  if (p.offsets == nullptr) {
+    if (lead) {
+      for (int ex = tid; ex < E; ex += 256) {
+        const int n = s_run[ex];
+        if (n > p.M_max) set_status(p.status, MOE_DEV_CAPACITY);
+        p.expert_num_tokens[ex] = (int32_t)min((int64_t)n, p.M_max);
+      }
+    }
+    for (int r = tid; r < R; r += 256) {
+      const int e = s_e[r];
+      const int slot = (e >= 0 && s_row[r] < p.M_max) ? s_row[r] : -1;
+      if (lead) p.route_slot[r] = slot;
+      s_row[r] = slot >= 0 ? (int32_t)(e * p.M_max + slot) : -1;
+    }
+  } else {
+    // contiguous layout: each expert's first row is the exclusive scan of
+    // the counts over the experts; thread i owns experts [i*per, i*per+per)
+    const int per = (E + 255) / 256;
+    const int e0 = tid * per;
+    int loc = 0;
+    for (int i = 0; i < per; ++i)
+      if (e0 + i < E) loc += s_run[e0 + i];
+    int incl = loc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
+    int first = wbase + incl - loc;
+    for (int i = 0; i < per; ++i) {
+      if (e0 + i >= E) break;
+      const int n = s_run[e0 + i];
+      if (lead) {
+        p.offsets[e0 + i] = first;
+        p.expert_num_tokens[e0 + i] = n;
+      }
+      s_run[e0 + i] = first;
+      first += n;
+    }
+    if (lead && tid == 255) p.offsets[E] = wbase + incl;
+    __syncthreads();
+    for (int r = tid; r < R; r += 256) {
+      const int e = s_e[r];
+      const int row = e >= 0 ? s_run[e] + s_row[r] : -1;
+      if (lead) p.route_slot[r] = row;
+      s_row[r] = row;
+    }
+  }
+  __syncthreads();
+  // The next kernel is let in only now: a GEMM block launched during the
+  // routing would take an SM that the routing's blocks still need, and the
+  // whole step runs 3-5 us longer that way.
+  pdl_launch_dependents();
+  quant_loop<SF_MODE, true, SHARED, true>(p, cur, gwarp, nwarps, tasks, lane, s_row);
+}
 
 // ---------------------------------------------------------------------------
 // NVFP4 token staging: per-token fp32 scale amax/2688, E2M1 codes with one
@@ -1127,6 +1286,20 @@ static moe_status_t launch_typed(StageParams& p, bool dispatch, int sf_mode, cud
   const bool ring = use_ring(p);
   if (dispatch) {
     const int64_t R = p.T * p.top_k;
+    if (!ring && R <= moe::kSmallRoutes && p.E * p.M_max < ((int64_t)1 << 31)) {
+      // a decode-sized batch: routing and quantisation in one launch
+      auto sk = sf_mode == MOE_SF_FP32
+                    ? moe::small_dispatch_kernel<MOE_SF_FP32, IdT, WT, false>
+                    : (p.shared_sf != nullptr
+                           ? moe::small_dispatch_kernel<MOE_SF_UE8M0_PACKED, IdT, WT, true>
+                           : moe::small_dispatch_kernel<MOE_SF_UE8M0_PACKED, IdT, WT, false>);
+      const size_t ssm = (size_t)5 * p.E * sizeof(int32_t);
+      cudaError_t le = launch_pdl(sk, dim3((unsigned)quant_grid(sk, tasks)), dim3(threads), ssm,
+                                  s, p);
+      if (le != cudaSuccess)
+        return set_error(MOE_ERR_CUDA, "small_dispatch_kernel launch: %s", cudaGetErrorString(le));
+      return MOE_OK;
+    }
     const int64_t B = (R + 1023) / 1024;
     p.num_route_blocks = B;
     const size_t smem = (size_t)32 * p.E * sizeof(uint16_t);

@@ -283,3 +283,83 @@ def test_shared_scale_pages_with_dispatch(cuda, orc):
     ref = orc.prepare_inputs(bf16_bits(hid), ids.numpy(), w.numpy())
     want = orc.shared_sf(ref["x_sf"], K, 96, rows=shared.shape[0], fill=0xEE)
     assert np.array_equal(shared, want)
+
+
+@pytest.mark.parametrize("T,K,k,idt,wdt,sf_mode,contiguous", [
+    # up to 1024 routes: routing and quantisation in one launch
+    (96, 640, 8, torch.int64, torch.bfloat16, B.MOE_SF_FP32, False),
+    (128, 1152, 8, torch.int32, torch.float32, B.MOE_SF_UE8M0_PACKED, True),
+    (1, 256, 3, torch.int32, torch.float32, B.MOE_SF_UE8M0_PACKED, False),
+    (1024, 256, 1, torch.int32, torch.float32, B.MOE_SF_UE8M0_PACKED, True),
+    # beyond: the routing kernel, then the quantisation
+    (129, 640, 8, torch.int64, torch.bfloat16, B.MOE_SF_FP32, False),
+    (300, 1152, 8, torch.int32, torch.float32, B.MOE_SF_UE8M0_PACKED, True),
+])
+def test_dispatch_with_eplb_both_paths(cuda, orc, T, K, k, idt, wdt, sf_mode, contiguous):
+    """Dispatch with EPLB replicas (load recorded, a tail of padded tokens
+    not counted), padding rows, either scale format and either layout, on
+    both sides of the one-launch limit: every output bit-exact with the
+    oracle."""
+    E_log = 32
+    hid = syn.make_hidden(T, K, 40 + T, outlier_frac=0.01, zero_group_frac=0.05)
+    ids, w, pad = syn.make_routing(T, E_log, k, 41 + T, zipf_s=1.1, padding_frac=0.05)
+    ids, w = ids.to(idt), w.to(wdt)
+    l2p, rc, nphys = syn.make_eplb(E_log, 42, two=6, three=3)
+    dev = torch.device("cuda")
+    unpadded = max(T - 3, 1)
+    load = torch.zeros(nphys, dtype=torch.int32, device=dev)
+    eplb = dict(logical_to_physical=l2p.to(dev), logical_replica_count=rc.to(dev),
+                expert_load=load, should_record=torch.ones(1, dtype=torch.uint8, device=dev),
+                num_unpadded_tokens=torch.tensor([unpadded], dtype=torch.int32, device=dev))
+    E = nphys
+    M_max = (T * k + E - 1) // E if contiguous else max(8, (T * k) // E)
+    G = K // 128
+    Wd = G if sf_mode == B.MOE_SF_FP32 else (G + 3) // 4
+    sf_dt = torch.float32 if sf_mode == B.MOE_SF_FP32 else torch.int32
+    rows_cap = E * M_max
+    x_b = torch.full((rows_cap, K), 0x5A, dtype=torch.uint8, device=dev)
+    sf_b = torch.full((rows_cap, Wd), -7, dtype=sf_dt, device=dev)
+    ent = torch.full((E,), -1, dtype=torch.int32, device=dev)
+    slot = torch.full((T, k), -9, dtype=torch.int32, device=dev)
+    ws = torch.empty(B.prepare_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    disp = dict(num_experts=E, max_tokens_per_expert=M_max, x_b=x_b, sf_b=sf_b,
+                expert_num_tokens=ent, route_slot=slot, workspace=ws)
+    offs = None
+    if contiguous:
+        offs = torch.full((E + 1,), -1, dtype=torch.int32, device=dev)
+        disp["expert_offsets"] = offs
+    x, x_sf, ids_out, w_out, st = _gpu_stage(hid, ids, w, pad, sf_mode=sf_mode, eplb=eplb,
+                                             dispatch=disp)
+    ref = orc.prepare_inputs(bf16_bits(hid), ids.numpy(), w.to(torch.float32).numpy(),
+                             is_padding=pad.numpy(), sf_mode=sf_mode, l2p=l2p.numpy(),
+                             replica_count=rc.numpy(), num_physical=nphys,
+                             record_enabled=True, num_unpadded=unpadded)
+    assert np.array_equal(ids_out, ref["ids"])
+    assert np.array_equal(w_out.view(np.uint32), ref["weights"].view(np.uint32))
+    assert np.array_equal(load.cpu().numpy(), ref["load"])
+    assert np.array_equal(u8(x), ref["x"])
+    sfw = x_sf.cpu().numpy()
+    assert np.array_equal(sfw.view(np.uint32), ref["x_sf"].view(np.uint32))
+    if contiguous:
+        d = orc.dispatch_contiguous(ref["ids"], ref["x"], ref["x_sf"], E)
+        assert np.array_equal(offs.cpu().numpy(), d["expert_offsets"])
+        assert np.array_equal(slot.cpu().numpy(), d["route_row"])
+        n_rows = int(d["expert_offsets"][-1])
+        xr, sfr = d["x_c"][:n_rows], d["sf_c"][:n_rows]
+        assert np.all(x_b.cpu().numpy()[n_rows:] == 0x5A)
+    else:
+        d = orc.dispatch(ref["ids"], ref["x"], ref["x_sf"], E, M_max)
+        assert np.array_equal(slot.cpu().numpy(), d["route_slot"])
+        rows = orc.valid_rows(d["expert_num_tokens"], M_max)
+        n_rows = len(rows)
+        xr, sfr = d["x_b"][rows], d["sf_b"][rows]
+    assert st == d["status"]
+    assert np.array_equal(ent.cpu().numpy(), d["expert_num_tokens"])
+    got_x = x_b.cpu().numpy()
+    got_sf = sf_b.cpu().numpy()
+    if contiguous:
+        got_x, got_sf = got_x[:n_rows], got_sf[:n_rows]
+    else:
+        got_x, got_sf = got_x[rows], got_sf[rows]
+    assert np.array_equal(got_x, xr)
+    assert np.array_equal(got_sf.view(np.uint32), np.asarray(sfr).view(np.uint32))
