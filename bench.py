@@ -54,12 +54,13 @@ GEMM_SRC = "moe_expert_layer_prepare_gb300/csrc/experts_gemm.cu"
 STAGING_SRC = "moe_expert_layer_prepare_gb300/csrc/staging.cu"
 COMMON_SRC = "moe_expert_layer_prepare_gb300/csrc/common.cuh"
 NCU_TRAFFIC = {
-    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (952.31e6, GEMM_SRC, "27b77fc5e84f75d5"),
-    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1040.37e6, GEMM_SRC,
-                                                       "27b77fc5e84f75d5"),
-    ("staging_stress", "quant_kernel<UE8M0,repack>"): (296.92e6, STAGING_SRC,
-                                                       "e7defe6027b3c631"),
-    ("staging_stress", "nvfp4_kernel"): (248.82e6, STAGING_SRC, "e7defe6027b3c631"),
+    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (945.65e6, GEMM_SRC, "bfb98cd9ef04b53e"),
+    ("deepseek_decode", "grouped_gemm_kernel<W13>"): (2023.35e6, GEMM_SRC, "bfb98cd9ef04b53e"),
+    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1092.25e6, GEMM_SRC,
+                                                       "bfb98cd9ef04b53e"),
+    ("staging_stress", "quant_ring_kernel<UE8M0,repack>"): (313.92e6, STAGING_SRC,
+                                                            "f229582db890d5a4"),
+    ("staging_stress", "nvfp4_ring_kernel"): (278.81e6, STAGING_SRC, "f229582db890d5a4"),
 }
 
 
