@@ -220,6 +220,15 @@ def algorithmic(wl):
                 w13_flops=4.0 * N * K * R, w2_flops=2.0 * N * K * R)
 
 
+def kernels_per_step(c):
+    """Library kernels one expert-layer step launches: a batch of at most 1024
+    routes (and fewer than 1024 tokens) stages and dispatches in one launch,
+    a longer one routes first and then quantises; then w13, w2, reduce."""
+    R = c["T"] * c["top_k"]
+    small = R <= 1024 and c["T"] < 1024 and c["E"] * c["M_max"] < (1 << 31)
+    return (1 if small else 2) + 3
+
+
 def config_of(name, wl, layout, stage_format, world):
     """The `config` object of a JSON line; both arms build it here, so that a
     workload is named identically whichever arm measured it."""
@@ -471,7 +480,7 @@ def bench_experts(name, args, world, dev, peaks, flush, want_cpu):
                e2e=dict(value=round(world * alg["flops"] / (e2e_ms * 1e-3) / 1e12, 3),
                         unit="TFLOP/s", h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
                         ms_per_step=round(e2e_ms, 4)),
-               gpu_launches=5 * K, clocks=ck)
+               gpu_launches=kernels_per_step(c) * K, clocks=ck)
     if want_cpu:
         n_tok = oracle_tokens_for(wl, 15.0)
         tm, thr, ntok = run_oracle_sample(wl, name, n_tok)
