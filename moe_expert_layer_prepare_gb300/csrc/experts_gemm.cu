@@ -98,8 +98,10 @@ struct GemmParams {
   uint8_t* y_sf_bytes;   // packed words viewed as bytes [E*M_max, 4*Wy]
   int Wy;
   uint16_t* h_dump;      // nullable bf16 [E*M_max, 2N]
+  int yq_al32;           // y_q 32-byte aligned: 32-byte row stores
   // w2 outputs
   uint16_t* out;         // bf16 [E*M_max, K]
+  int out_al32;          // out 32-byte aligned: 32-byte row stores
   float* partials;       // [splits, E*M_max, K]
   int32_t* counters;     // [(E * mt_max + E) * n_tiles]
   int mt_max;
@@ -811,14 +813,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float inv = ue8m0_inverse(code);
         if (row_ok) {
           uint8_t* dst = p.y_q + grow * (int64_t)p.N + n0;
+          // the row's 64 codes: two 32-byte stores when y_q allows, else four
+          // 16-byte ones (each thread writes its own row)
+          if (p.yq_al32) {
 #pragma unroll
-          for (int i = 0; i < 64; i += 16) {
-            uint4 v;
-            v.x = pack4_e4m3(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv, acc[i + 3] * inv);
-            v.y = pack4_e4m3(acc[i + 4] * inv, acc[i + 5] * inv, acc[i + 6] * inv, acc[i + 7] * inv);
-            v.z = pack4_e4m3(acc[i + 8] * inv, acc[i + 9] * inv, acc[i + 10] * inv, acc[i + 11] * inv);
-            v.w = pack4_e4m3(acc[i + 12] * inv, acc[i + 13] * inv, acc[i + 14] * inv, acc[i + 15] * inv);
-            st_v4(dst + i, v);
+            for (int i = 0; i < 64; i += 32) {
+              uint32_t v[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                v[j] = pack4_e4m3(acc[i + 4 * j] * inv, acc[i + 4 * j + 1] * inv,
+                                  acc[i + 4 * j + 2] * inv, acc[i + 4 * j + 3] * inv);
+              st_v8(dst + i, v);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; i += 16) {
+              uint4 v;
+              v.x = pack4_e4m3(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv, acc[i + 3] * inv);
+              v.y = pack4_e4m3(acc[i + 4] * inv, acc[i + 5] * inv, acc[i + 6] * inv,
+                               acc[i + 7] * inv);
+              v.z = pack4_e4m3(acc[i + 8] * inv, acc[i + 9] * inv, acc[i + 10] * inv,
+                               acc[i + 11] * inv);
+              v.w = pack4_e4m3(acc[i + 12] * inv, acc[i + 13] * inv, acc[i + 14] * inv,
+                               acc[i + 15] * inv);
+              st_v4(dst + i, v);
+            }
           }
           if (h == 0) p.y_sf_bytes[grow * (int64_t)(4 * p.Wy) + w.nt] = (uint8_t)code;
         }
@@ -829,14 +848,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (p.splits == 1) {
           if (row_ok && cols_ok) {
             uint16_t* dst = p.out + grow * (int64_t)p.K + c0;
+            // Each thread writes its own row, so a warp's store touches 32
+            // rows; 32-byte stores fill whole sectors and halve the store
+            // instructions (prefill w2 -10% against 16-byte stores).
+            if (p.out_al32) {
 #pragma unroll
-            for (int i = 0; i < 128; i += 8) {
-              uint4 v;
-              v.x = f32_to_bf16_bits(acc[i]) | (f32_to_bf16_bits(acc[i + 1]) << 16);
-              v.y = f32_to_bf16_bits(acc[i + 2]) | (f32_to_bf16_bits(acc[i + 3]) << 16);
-              v.z = f32_to_bf16_bits(acc[i + 4]) | (f32_to_bf16_bits(acc[i + 5]) << 16);
-              v.w = f32_to_bf16_bits(acc[i + 6]) | (f32_to_bf16_bits(acc[i + 7]) << 16);
-              st_v4(dst + i, v);
+              for (int i = 0; i < 128; i += 16) {
+                uint32_t v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  v[j] = f32_to_bf16_bits(acc[i + 2 * j]) |
+                         (f32_to_bf16_bits(acc[i + 2 * j + 1]) << 16);
+                st_v8(dst + i, v);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 128; i += 8) {
+                uint4 v;
+                v.x = f32_to_bf16_bits(acc[i]) | (f32_to_bf16_bits(acc[i + 1]) << 16);
+                v.y = f32_to_bf16_bits(acc[i + 2]) | (f32_to_bf16_bits(acc[i + 3]) << 16);
+                v.z = f32_to_bf16_bits(acc[i + 4]) | (f32_to_bf16_bits(acc[i + 5]) << 16);
+                v.w = f32_to_bf16_bits(acc[i + 6]) | (f32_to_bf16_bits(acc[i + 7]) << 16);
+                st_v4(dst + i, v);
+              }
             }
           }
         } else {
@@ -1086,6 +1120,8 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
     p.Wa = af32 ? (int)(K / 128) : (int)((K / 128 + 3) / 4);
     p.w_s = a->w13_scale;
     p.y_q = inter_q;
+    // rows of N bytes (N a multiple of 128) and column blocks of 64 bytes
+    p.yq_al32 = (reinterpret_cast<uintptr_t>(inter_q) & 31u) == 0 ? 1 : 0;
     p.y_sf_bytes = reinterpret_cast<uint8_t*>(inter_sf);
     p.Wy = (int)Wy;
     p.h_dump = static_cast<uint16_t*>(a->gate_up_dump);
@@ -1125,6 +1161,8 @@ moe_status_t launch_experts(const moe_experts_args_t* a, cudaStream_t s) {
     p.Wa = (int)Wy;
     p.w_s = a->w2_scale;
     p.out = static_cast<uint16_t*>(a->output);
+    // rows of 2K bytes (K a multiple of 128) and column blocks of 256 bytes
+    p.out_al32 = (reinterpret_cast<uintptr_t>(a->output) & 31u) == 0 ? 1 : 0;
     p.partials = partials;
     p.counters = counters;
     p.mt_max = (int)mt_max;

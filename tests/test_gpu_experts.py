@@ -204,3 +204,42 @@ def test_full_size_sampled(cuda, orc, name, n_tok):
     if pad.any():
         assert np.all(bf16_bits(layer.out)[np.nonzero(pad)[0]] == 0), \
             "padding tokens must be unrouted"
+
+
+def test_outputs_at_16_byte_offsets(cuda, orc):
+    """The ABI asks only 16-byte alignment of the expert output and of an
+    explicit inter_q.  Both GEMMs store their rows with 32-byte stores when the
+    buffer allows and with 16-byte stores otherwise; the two forms write the
+    same bytes.  Run once into 32-byte-aligned buffers and once into views
+    16 bytes past a 256-byte boundary, and compare every valid row bit for bit."""
+    T, K, N, E, k, M = 250, 384, 256, 3, 2, 300
+    wl = _custom_workload(T, K, N, E, k, M, seed=77)
+    layer = _layer(wl, cuda)
+    layer.prepare(wl["hidden"].to(cuda), wl["topk_ids"].to(cuda), wl["topk_weights"].to(cuda),
+                  wl["is_padding"].to(cuda))
+    G = N // 128
+    Wy = (G + 3) // 4
+
+    def run(off):
+        raw_o = torch.zeros(E * M * K * 2 + 64, dtype=torch.uint8, device=cuda)
+        raw_q = torch.zeros(E * M * N + 64, dtype=torch.uint8, device=cuda)
+        out_b = raw_o[32 + off:32 + off + E * M * K * 2].view(torch.bfloat16).view(E * M, K)
+        inter_q = raw_q[32 + off:32 + off + E * M * N].view(E * M, N)
+        assert out_b.data_ptr() % 32 == off and inter_q.data_ptr() % 32 == off
+        inter_sf = torch.zeros((E * M, Wy), dtype=torch.int32, device=cuda)
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        B.moe_batched_experts(out_b, layer.x_b, layer.sf_b, layer.w13, layer.w13_s, layer.w2,
+                              layer.w2_s, layer.expert_num_tokens, layer.ws13, layer.ws2,
+                              valid_shape_m=layer.valid_shape_m, inter_q=inter_q,
+                              inter_sf=inter_sf, device_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        return bf16_bits(out_b), inter_q.cpu().numpy(), inter_sf.cpu().numpy()
+
+    o32, q32, s32 = run(0)
+    o16, q16, s16 = run(16)
+    rows = orc.valid_rows(layer.expert_num_tokens.cpu().numpy(), M)
+    assert len(rows) > 0
+    assert np.array_equal(q16[rows], q32[rows])
+    assert np.array_equal(s16[rows], s32[rows])
+    assert np.array_equal(o16[rows], o32[rows])
