@@ -54,13 +54,13 @@ GEMM_SRC = "moe_expert_layer_prepare_gb300/csrc/experts_gemm.cu"
 STAGING_SRC = "moe_expert_layer_prepare_gb300/csrc/staging.cu"
 COMMON_SRC = "moe_expert_layer_prepare_gb300/csrc/common.cuh"
 NCU_TRAFFIC = {
-    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (945.65e6, GEMM_SRC, "bfb98cd9ef04b53e"),
-    ("deepseek_decode", "grouped_gemm_kernel<W13>"): (2023.35e6, GEMM_SRC, "bfb98cd9ef04b53e"),
-    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1092.25e6, GEMM_SRC,
-                                                       "bfb98cd9ef04b53e"),
-    ("staging_stress", "quant_ring_kernel<UE8M0,repack>"): (313.92e6, STAGING_SRC,
-                                                            "f229582db890d5a4"),
-    ("staging_stress", "nvfp4_ring_kernel"): (278.81e6, STAGING_SRC, "f229582db890d5a4"),
+    ("mixtral_decode", "grouped_gemm_kernel<W13>"): (945.67e6, GEMM_SRC, "135943ea8fb0e0c9"),
+    ("deepseek_decode", "grouped_gemm_kernel<W13>"): (2023.44e6, GEMM_SRC, "135943ea8fb0e0c9"),
+    ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1159.99e6, GEMM_SRC,
+                                                       "135943ea8fb0e0c9"),
+    ("staging_stress", "quant_ring_kernel<UE8M0,repack>"): (314.08e6, STAGING_SRC,
+                                                            "4cf6cba7515737b5"),
+    ("staging_stress", "nvfp4_ring_kernel"): (279.00e6, STAGING_SRC, "4cf6cba7515737b5"),
 }
 
 
