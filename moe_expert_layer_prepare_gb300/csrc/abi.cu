@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -18,36 +19,46 @@ moe_status_t set_error(moe_status_t st, const char* fmt, ...) {
   return st;
 }
 
+// SM count and occupancy queries, cached per device (and per kernel and
+// block size) under one lock: concurrent first calls from several host
+// threads, or on several devices, all see complete entries.
+static std::mutex g_query_mu;
+
 int num_sms() {
   static int cached[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  std::lock_guard<std::mutex> lock(g_query_mu);
   if (cached[dev] == 0) {
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 148;
+      v = 152;
     cached[dev] = v;
   }
   return cached[dev];
 }
 
-// Resident blocks per SM of a kernel at a block size (cached per kernel).
+// Resident blocks per SM of a kernel at a block size with no dynamic shared
+// memory.  When the table is full the query is made each time.
 int resident_blocks(const void* kernel, int block) {
-  static const void* keys[32] = {};
-  static int vals[32] = {};
-  for (int i = 0; i < 32; ++i) {
-    if (keys[i] == kernel) return vals[i];
-    if (keys[i] == nullptr) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, 0) != cudaSuccess ||
-          n < 1)
-        n = 1;
-      keys[i] = kernel;
-      vals[i] = n;
-      return n;
-    }
-  }
-  return 1;
+  struct Entry {
+    const void* kernel;
+    int block, dev, blocks;
+  };
+  constexpr int kEntries = 256;
+  static Entry table[kEntries] = {};
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  std::lock_guard<std::mutex> lock(g_query_mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].kernel == kernel && table[i].block == block && table[i].dev == dev)
+      return table[i].blocks;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, 0) != cudaSuccess || n < 1)
+    n = 1;
+  if (used < kEntries) table[used++] = Entry{kernel, block, dev, n};
+  return n;
 }
 
 size_t prepare_workspace_size(int64_t T, int64_t k, int64_t E);
