@@ -243,3 +243,44 @@ def test_outputs_at_16_byte_offsets(cuda, orc):
     assert np.array_equal(q16[rows], q32[rows])
     assert np.array_equal(s16[rows], s32[rows])
     assert np.array_equal(o16[rows], o32[rows])
+
+
+def test_whole_step_replays_from_a_cuda_graph(cuda, orc):
+    """The host never reads device data between the calls, so the whole step
+    (staging + dispatch, both GEMMs, reduce) can be captured once and replayed
+    on new inputs copied into the captured buffers.  Each replay must equal a
+    direct run on the same inputs, bit for bit."""
+    T, K, N, E, k, M = 96, 512, 256, 8, 2, 64
+    wls = [_custom_workload(T, K, N, E, k, M, seed=s) for s in (501, 502, 503)]
+    # one set of weights: the experts stay, the batches change
+    for w in wls[1:]:
+        for n in ("w13", "w13_s", "w2", "w2_s"):
+            w[n] = wls[0][n]
+    layer = _layer(wls[0], cuda)
+    bufs = [wls[0][n].to(cuda) for n in ("hidden", "topk_ids", "topk_weights", "is_padding")]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            layer.forward(*bufs)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(*bufs)
+    torch.cuda.synchronize()
+    for wl in wls:
+        for dst, n in zip(bufs, ("hidden", "topk_ids", "topk_weights", "is_padding")):
+            dst.copy_(wl[n].to(cuda))
+        layer.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        replayed = layer.out.clone()
+        layer.forward(*bufs)
+        torch.cuda.synchronize()
+        assert int(layer.status.item()) == 0
+        assert torch.equal(replayed, layer.out)
+    # and the last replay is the oracle's result
+    ref = orc.forward(bf16_bits(wls[-1]["hidden"]), wls[-1]["topk_ids"].numpy(),
+                      wls[-1]["topk_weights"].numpy(),
+                      *[wls[-1][n].numpy() for n in ("w13", "w13_s", "w2", "w2_s")], E, M, N,
+                      is_padding=wls[-1]["is_padding"].numpy())
+    assert_fp_close(bf16_vals(bf16_bits(replayed)), bf16_vals(ref["out"]), "graph replay output")
