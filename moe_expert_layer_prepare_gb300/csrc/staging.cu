@@ -551,11 +551,13 @@ __global__ void __launch_bounds__(256) quant_kernel(StageParams p) {
   const bool recorded = REPACK && record_on && p.load != nullptr && p.num_physical <= kLoadBins;
   const int64_t nrep = recorded ? min((int64_t)gridDim.x, (int64_t)kLoadBlocks) : 0;
   const bool set_aside = recorded && gridDim.x >= 4 * kLoadBlocks;
-  if (REPACK && set_aside && blockIdx.x < nrep) {
-    const int64_t per = (R + nrep - 1) / nrep;
-    repack_recorded<IdT, WT>(p, blockIdx.x * per, min(R, (blockIdx.x + 1) * per), unpadded,
-                             s_load);
-    return;
+  if constexpr (REPACK) {
+    if (set_aside && blockIdx.x < nrep) {
+      const int64_t per = (R + nrep - 1) / nrep;
+      repack_recorded<IdT, WT>(p, blockIdx.x * per, min(R, (blockIdx.x + 1) * per), unpadded,
+                               s_load);
+      return;
+    }
   }
   const int64_t sblock = set_aside ? blockIdx.x - nrep : blockIdx.x;
   const int64_t sgrid = set_aside ? gridDim.x - nrep : gridDim.x;
