@@ -1265,12 +1265,36 @@ constexpr int64_t kRingMinTokens = 1024;
 
 static bool use_ring(const StageParams& p) { return p.K <= 8192 && p.T >= kRingMinTokens; }
 
+// Row warps per block of a ring kernel: as many as the row buffers fit next
+// to the load histogram in 227 KB (at most RING_MAX_WARPS), or up to four
+// fewer when that deals the rows out in fuller rounds.  The rows go to
+// blocks x warps in rounds, and a round takes about as long as the warps
+// sharing an SM's bandwidth, so the cost is rounds x warps: 16,384 rows on
+// 152 SMs take 8 rounds of 14 (112) or 9 of 12 (108).
+static int ring_row_warps(int64_t T, int64_t K) {
+  const size_t rowbytes = (size_t)(K * 2);
+  const size_t hist = (size_t)moe::kLoadBins * sizeof(int);
+  int wmax = (int)((227 * 1024 - 1024 - hist) / rowbytes);
+  if (wmax > moe::RING_MAX_WARPS) wmax = moe::RING_MAX_WARPS;
+  if (wmax < 1) wmax = 1;
+  const int64_t sms = num_sms();
+  int best = wmax;
+  int64_t best_cost = (T + sms * wmax - 1) / (sms * wmax) * wmax;
+  for (int w = wmax - 1; w >= 1 && w >= wmax - 4; --w) {
+    const int64_t cost = (T + sms * w - 1) / (sms * w) * w;
+    if (cost < best_cost) {
+      best = w;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 template <typename Kernel>
 static cudaError_t launch_ring(Kernel k, const StageParams& p, cudaStream_t s) {
   const size_t rowbytes = (size_t)(p.K * 2);
   const size_t hist = (size_t)moe::kLoadBins * sizeof(int);
-  int row_warps = (int)((227 * 1024 - 1024 - hist) / rowbytes);
-  if (row_warps > moe::RING_MAX_WARPS) row_warps = moe::RING_MAX_WARPS;
+  const int row_warps = ring_row_warps(p.T, p.K);
   const size_t smem = (size_t)row_warps * rowbytes + hist;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -1475,8 +1499,7 @@ static moe_status_t launch_nvfp4_typed(const moe::Nvfp4Params& q, const StagePar
     // 640 bytes) in 227 KB of shared memory
     const size_t rowbytes = (size_t)(q.K * 2);
     const size_t hist = (size_t)moe::kLoadBins * sizeof(int);
-    int row_warps = (int)((227 * 1024 - 1024 - hist) / rowbytes);
-    if (row_warps > moe::RING_MAX_WARPS) row_warps = moe::RING_MAX_WARPS;
+    const int row_warps = ring_row_warps(q.T, q.K);
     const size_t smem = (size_t)row_warps * rowbytes + hist;
     cudaError_t ae = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (ae != cudaSuccess)
