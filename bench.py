@@ -58,9 +58,9 @@ NCU_TRAFFIC = {
     ("deepseek_decode", "grouped_gemm_kernel<W13>"): (2023.44e6, GEMM_SRC, "135943ea8fb0e0c9"),
     ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1159.99e6, GEMM_SRC,
                                                        "135943ea8fb0e0c9"),
-    ("staging_stress", "quant_ring_kernel<UE8M0,repack>"): (313.65e6, STAGING_SRC,
-                                                            "55803d774d53d0ae"),
-    ("staging_stress", "nvfp4_ring_kernel"): (278.70e6, STAGING_SRC, "55803d774d53d0ae"),
+    ("staging_stress", "quant_ring_kernel<UE8M0,repack>"): (316.70e6, STAGING_SRC,
+                                                            "7cf6f0f150d73828"),
+    ("staging_stress", "nvfp4_ring_kernel"): (279.41e6, STAGING_SRC, "7cf6f0f150d73828"),
 }
 
 
