@@ -8,19 +8,27 @@
 // BatchedHummingGroupedExperts ("...fused_moe.experts.fused_humming_moe").
 //
 // Kernels
+//   small_dispatch_kernel : a batch of at most 1024 routes with dispatch, in
+//                  one launch: every block ranks all routes in shared memory,
+//                  then quantises its tasks and scatters them.
 //   route_kernel : one thread per route (t, j), 1024 routes per block.  Repack
 //                  + EPLB + per-block expert histogram + the stable rank of the
 //                  route among the block's routes to the same expert.  The last
 //                  block to finish turns the histograms into per-block
 //                  exclusive offsets (column scan over blocks) and writes
 //                  expert_num_tokens.
-//   quant_kernel : one warp per (token, 4 groups = 512 elements): two
-//                  16-byte loads per lane, each covering 512 contiguous bytes
-//                  per warp, warp-shuffle amax over the 16 lanes of a group,
-//                  packed fp8 stores, one packed exponent word per task;
-//                  optionally the same bytes are stored into each routed slot
-//                  of x_b.
-//                  Without dispatch the repack is folded into this kernel.
+//   quant_ring_kernel : batches of 1024 tokens or more: rows stream through
+//                  shared-memory buffers filled by bulk copies, one per row
+//                  warp, with two routing warps repacking alongside.
+//   quant_kernel : shorter batches: one warp per (token, 4 groups = 512
+//                  elements): two 16-byte loads per lane, each covering 512
+//                  contiguous bytes per warp, warp-shuffle amax over the 16
+//                  lanes of a group, packed fp8 stores, one packed exponent
+//                  word per task; optionally the same bytes are stored into
+//                  each routed slot of x_b.
+//   nvfp4_ring_kernel / nvfp4_kernel : the NVFP4 token staging, in the same
+//                  two forms.
+//                  Without dispatch the repack is folded into the quantiser.
 #include <cstdio>
 #include <type_traits>
 
