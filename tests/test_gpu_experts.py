@@ -134,6 +134,8 @@ def test_tiny_full(cuda, orc):
     (250, 384, 256, 3, 2, 300),
     # w2 split of the reduction (valid_shape_m hint forces several splits)
     (40, 1024, 2048, 8, 2, 64),
+    # the most experts the GEMMs take (1024), most of them empty
+    (64, 256, 256, 1024, 4, 8),
 ])
 def test_ragged_and_split(cuda, orc, shape):
     T, K, N, E, k, M = shape

@@ -156,6 +156,8 @@ def _dispatch_case(T, K, k, E, M_max, zipf=None, pad_frac=0.0, seed=0):
     (128, 7168, 8, 256, 128, 1.1, 0.02),      # deepseek decode routing
     (300, 384, 8, 64, 300, None, 0.1),        # 3 route blocks, ragged
     (8192, 256, 8, 256, 1024, None, 0.0),     # deepseek prefill routing (narrow K)
+    (120, 256, 8, 1024, 8, None, 0.0),        # the most experts, one-launch path
+    (600, 256, 8, 1024, 32, None, 0.05),      # the most experts, routing kernel
 ])
 def test_dispatch(cuda, orc, T, K, k, E, M_max, zipf, pad_frac):
     hid, ids, w, pad = _dispatch_case(T, K, k, E, M_max, zipf, pad_frac, seed=T + E)
