@@ -286,3 +286,30 @@ def test_whole_step_replays_from_a_cuda_graph(cuda, orc):
                       *[wls[-1][n].numpy() for n in ("w13", "w13_s", "w2", "w2_s")], E, M, N,
                       is_padding=wls[-1]["is_padding"].numpy())
     assert_fp_close(bf16_vals(bf16_bits(replayed)), bf16_vals(ref["out"]), "graph replay output")
+
+
+@pytest.mark.parametrize("chunks", [None, 1, 3])
+def test_forward_from_host_buffers(cuda, orc, chunks):
+    """The end-to-end call from pinned host buffers (inputs copied in, the
+    reduce in token chunks whose rows are copied back while the next chunk is
+    reduced) returns exactly the device path's output, on a stream of its
+    own and back to back."""
+    T, K, N, E, k, M = 1200, 256, 256, 8, 2, 400
+    wls = [_custom_workload(T, K, N, E, k, M, seed=s) for s in (611, 612)]
+    for n in ("w13", "w13_s", "w2", "w2_s"):
+        wls[1][n] = wls[0][n]
+    layer = _layer(wls[0], cuda)
+    s = torch.cuda.Stream()
+    outs = []
+    for wl in wls:
+        host = [wl[n].pin_memory() for n in ("hidden", "topk_ids", "topk_weights", "is_padding")]
+        out_h = torch.empty((T, K), dtype=torch.bfloat16).pin_memory()
+        layer.forward_host(*host, out_h, stream=s, chunks=chunks)
+        outs.append(out_h)
+    s.synchronize()
+    for wl, out_h in zip(wls, outs):
+        ref = layer.forward(*[wl[n].to(cuda) for n in ("hidden", "topk_ids", "topk_weights",
+                                                       "is_padding")])
+        torch.cuda.synchronize()
+        assert int(layer.status.item()) == 0
+        assert torch.equal(out_h, ref.cpu())
