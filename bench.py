@@ -59,9 +59,9 @@ NCU_TRAFFIC = {
     ("deepseek_decode", "grouped_gemm_kernel<W13>"): (2023.44e6, GEMM_SRC, "ee740f19ec2b65ed"),
     ("deepseek_prefill", "grouped_gemm_kernel<W13>"): (8 * 1159.99e6, GEMM_SRC,
                                                        "ee740f19ec2b65ed"),
-    ("staging_stress", "quant_ring_kernel<UE8M0,repack>"): (316.70e6, STAGING_SRC,
-                                                            "b23c1394f6431074"),
-    ("staging_stress", "nvfp4_ring_kernel"): (279.41e6, STAGING_SRC, "b23c1394f6431074"),
+    ("staging_stress", "quant_ring_kernel<UE8M0,repack>"): (316.96e6, STAGING_SRC,
+                                                            "77a3e2abe55e3692"),
+    ("staging_stress", "nvfp4_ring_kernel"): (279.43e6, STAGING_SRC, "77a3e2abe55e3692"),
 }
 
 
@@ -107,6 +107,11 @@ def parse(argv=None):
                     help="staging_stress: 1x128 UE8M0 fp8 staging or NVFP4 token staging")
     ap.add_argument("--layout", default="batched", choices=["batched", "contiguous"],
                     help="expert row layout: [E, M_max] slots or expert_offsets")
+    ap.add_argument("--act-scales", default="ue8m0", choices=["ue8m0", "fp32"],
+                    help="expert layers: 1x128 activation scales as packed UE8M0 or fp32")
+    ap.add_argument("--shared-block-m", type=int, default=0,
+                    help="staging_stress: also write the shared-expert scale pages of this "
+                         "block size (NVFP4: the MXFP8 shared input, fp8 rows + pages)")
     return ap.parse_args(argv)
 
 
@@ -208,7 +213,7 @@ def routing_counts(wl):
     return int(routed.size), int(np.unique(routed).size)
 
 
-def algorithmic(wl):
+def algorithmic(wl, fp32_scales=False):
     """Valid-row FLOPs and algorithmic bytes per kernel.
 
     FLOPs count routed rows only (6*N*K per route: 4*N*K in w13, 2*N*K in w2).
@@ -221,10 +226,11 @@ def algorithmic(wl):
     R, A = routing_counts(wl)
     G, Gn = K // 128, N // 128
     Wa, Wy = (G + 3) // 4, (Gn + 3) // 4
-    w13_bytes = A * (2 * N * K + (2 * N // 128) * G * 4) + R * (K + 4 * Wa) + R * (N + Gn) + 4 * E
+    Sa = 4 * G if fp32_scales else 4 * Wa  # one row's activation scale bytes
+    w13_bytes = A * (2 * N * K + (2 * N // 128) * G * 4) + R * (K + Sa) + R * (N + Gn) + 4 * E
     w2_bytes = A * (K * N + (K // 128) * Gn * 4) + R * (N + 4 * Wy) + R * K * 2 + 4 * E
-    stage_bytes = T * K * 2 + T * k * 8 + T + T * K + T * 4 * Wa + T * k * 8 + T * k * 4 + \
-        R * (K + 4 * Wa) + R * 4 + E * 4
+    stage_bytes = T * K * 2 + T * k * 8 + T + T * K + T * Sa + T * k * 8 + T * k * 4 + \
+        R * (K + Sa) + R * 4 + E * 4
     reduce_bytes = R * K * 2 + T * K * 2 + T * k * (8 + 4 + 4)
     return dict(R=R, A=A, flops=6.0 * N * K * R, w13_bytes=w13_bytes, w2_bytes=w2_bytes,
                 stage_bytes=stage_bytes, reduce_bytes=reduce_bytes,
@@ -240,19 +246,27 @@ def kernels_per_step(c):
     return (1 if small else 2) + 3
 
 
-def config_of(name, wl, layout, stage_format, world):
+def config_of(name, wl, layout, stage_format, world, args=None):
     """The `config` object of a JSON line; both arms build it here, so that a
-    workload is named identically whichever arm measured it."""
+    workload is named identically whichever arm measured it.  Options that
+    change the work (fp32 activation scales, shared-expert pages) are named
+    in it when set."""
     c = wl["cfg"]
     if c.get("N") is None:
-        return dict(workload=name, format=stage_format, T=c["T"], K=c["K"], top_k=c["top_k"],
-                    experts_logical=c["E"], experts_physical=wl["num_physical"], l2=L2_NOTE,
-                    parallelism=f"replicas x{world}")
+        out = dict(workload=name, format=stage_format, T=c["T"], K=c["K"], top_k=c["top_k"],
+                   experts_logical=c["E"], experts_physical=wl["num_physical"], l2=L2_NOTE,
+                   parallelism=f"replicas x{world}")
+        if args is not None and args.shared_block_m > 0:
+            out["shared_block_m"] = args.shared_block_m
+        return out
     R, A = routing_counts(wl)
     M_max = max(1, -(-(c["T"] * c["top_k"]) // c["E"])) if layout == "contiguous" else c["M_max"]
-    return dict(workload=name, T=c["T"], K=c["K"], N=c["N"], E=c["E"], top_k=c["top_k"],
-                M_max=M_max, layout=layout, routed_rows=R, active_experts=A, l2=L2_NOTE,
-                parallelism=f"replicas x{world}")
+    out = dict(workload=name, T=c["T"], K=c["K"], N=c["N"], E=c["E"], top_k=c["top_k"],
+               M_max=M_max, layout=layout, routed_rows=R, active_experts=A, l2=L2_NOTE,
+               parallelism=f"replicas x{world}")
+    if args is not None and args.act_scales != "ue8m0":
+        out["act_scales"] = args.act_scales
+    return out
 
 
 def median(xs):
@@ -323,12 +337,14 @@ def run_oracle_nvfp4(wl, n_tok):
     return time.perf_counter() - t0, oracle.num_threads(), n
 
 
-def staging_bytes(T, K, k, wl, nvfp4=False):
+def staging_bytes(T, K, k, wl, nvfp4=False, shared_pages=False):
     G = K // 128
     b = T * K * 2 + T * k * 4 * 2 + T * K + T * 4 * ((G + 3) // 4) + T * k * 12 + \
         wl["l2p"].numel() * 4 + wl["replica_count"].numel() * 4
     if nvfp4:  # codes K/2 + E4M3 scales K/16 + fp32 scale, instead of K + K/32
         b += T * (K // 2 + K // 16 + 4) - T * (K + 4 * ((G + 3) // 4))
+    if shared_pages:  # one exponent byte per group; NVFP4 also writes the fp8 rows
+        b += T * G + (T * K if nvfp4 else 0)
     return b
 
 
@@ -374,10 +390,11 @@ def bench_experts(name, args, world, dev, peaks, flush, want_cpu):
     wl = build_workload(name, dev)
     c = wl["cfg"]
     s = torch.cuda.current_stream()
-    alg = algorithmic(wl)
+    fp32_scales = args.act_scales == "fp32"
+    alg = algorithmic(wl, fp32_scales=fp32_scales)
     layer = B.MoeLayer(c["T"], c["K"], c["N"], c["E"], c["top_k"], c["M_max"], wl["w13"],
                        wl["w13_s"], wl["w2"], wl["w2_s"], device=dev,
-                       contiguous=args.layout == "contiguous")
+                       contiguous=args.layout == "contiguous", fp32_scales=fp32_scales)
     hid, ids, wts, pad = (wl["hidden"].to(dev), wl["topk_ids"].to(dev),
                           wl["topk_weights"].to(dev), wl["is_padding"].to(dev))
     inter_q, inter_sf = layer.inter()
@@ -475,7 +492,7 @@ def bench_experts(name, args, world, dev, peaks, flush, want_cpu):
     assert int(layer.status.item()) == 0, "device status set during the timed steps"
     out = dict(value=round(value, 3), unit="TFLOP/s", ms_per_step=round(ms, 4),
                dtype="fp8e4m3 (fp32 accumulate)",
-               config=config_of(name, wl, args.layout, "fp8", world), roofline=roof,
+               config=config_of(name, wl, args.layout, "fp8", world, args), roofline=roof,
                stages_ms=dict(prepare=round(med[0], 4), w13=round(med[1], 4),
                               w2=round(med[2], 4), reduce=round(med[3], 4),
                               note="separate pass, events between the calls",
@@ -528,12 +545,23 @@ def bench_staging(args, world, dev, peaks, flush, want_cpu, fmt):
                                                                         device=dev),
                 num_unpadded_tokens=torch.tensor([T], dtype=torch.int32, device=dev))
     s = torch.cuda.current_stream()
+    # optional shared-expert pages (and, for NVFP4, the MXFP8 shared input)
+    bm = args.shared_block_m
+    pages = shared_q = None
+    if bm > 0:
+        rows = (T + bm - 1) // bm * ((bm + 127) // 128 * 128)
+        pages = torch.empty((rows, G), dtype=torch.uint8, device=dev)
+        if nvfp4:
+            shared_q = torch.empty((T, K), dtype=torch.uint8, device=dev)
 
     def run():
         if nvfp4:
-            B.moe_prepare_nvfp4_inputs(hid, ids, wts, x, x_sf, x_scales, io, wo, eplb=eplb)
+            B.moe_prepare_nvfp4_inputs(hid, ids, wts, x, x_sf, x_scales, io, wo, eplb=eplb,
+                                       shared_x=shared_q, shared_x_sf=pages,
+                                       shared_block_m=bm if bm > 0 else None)
         else:
-            B.moe_prepare_inputs(hid, ids, wts, x, x_sf, io, wo, eplb=eplb)
+            B.moe_prepare_inputs(hid, ids, wts, x, x_sf, io, wo, eplb=eplb, shared_x_sf=pages,
+                                 shared_block_m=bm if bm > 0 else None)
 
     def step(evs):
         if evs:
@@ -551,13 +579,13 @@ def bench_staging(args, world, dev, peaks, flush, want_cpu, fmt):
     t = timed_steps(step, Ks, s, 2, flush, world)[:, 0]
     ck = clocks.stop()
     ms = max_over_ranks(world, median(t))
-    nbytes = staging_bytes(T, K, k, wl, nvfp4)
+    nbytes = staging_bytes(T, K, k, wl, nvfp4, shared_pages=bm > 0)
     gbs = world * nbytes / (ms * 1e-3) / 1e9
     kern = "nvfp4_ring_kernel" if nvfp4 else "quant_ring_kernel<UE8M0,repack>"
     out = dict(value=round(gbs, 1), unit="GB/s", ms_per_step=round(ms, 4),
                dtype="bf16->e2m1 (e4m3/16, fp32/token)" if nvfp4 else
                "bf16->fp8e4m3 (fp32 scale math)",
-               config=config_of("staging_stress", wl, "batched", fmt, world),
+               config=config_of("staging_stress", wl, "batched", fmt, world, args),
                roofline=dict(bound="hbm", achieved=round(gbs / world, 1), peak=peaks["hbm"],
                              unit="GB/s", frac=round(gbs / world / peaks["hbm"], 4),
                              traffic=ncu_traffic("staging_stress", kern), kernel=kern,
@@ -663,7 +691,7 @@ def bench_reference(args, world, rank):
     c = wl["cfg"]
     # each step is a bounded sample so that the whole run stays near 90 s
     per_step_s = max(0.05, min(2.0, 90.0 / max(args.steps + args.warmup, 1)))
-    config = config_of(args.config, wl, args.layout, args.stage_format, world)
+    config = config_of(args.config, wl, args.layout, args.stage_format, world, args)
     if staging:
         return bench_reference_staging(args, world, wl, per_step_s, config)
     n_tok = oracle_tokens_for(wl, per_step_s)
