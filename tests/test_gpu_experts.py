@@ -288,8 +288,9 @@ def test_whole_step_replays_from_a_cuda_graph(cuda, orc):
     assert_fp_close(bf16_vals(bf16_bits(replayed)), bf16_vals(ref["out"]), "graph replay output")
 
 
-@pytest.mark.parametrize("chunks", [None, 1, 3])
-def test_forward_from_host_buffers(cuda, orc, chunks):
+@pytest.mark.parametrize("chunks,contiguous", [(None, False), (1, False), (3, False),
+                                               (None, True)])
+def test_forward_from_host_buffers(cuda, orc, chunks, contiguous):
     """The end-to-end call from pinned host buffers (inputs copied in, the
     reduce in token chunks whose rows are copied back while the next chunk is
     reduced) returns exactly the device path's output, on a stream of its
@@ -298,7 +299,12 @@ def test_forward_from_host_buffers(cuda, orc, chunks):
     wls = [_custom_workload(T, K, N, E, k, M, seed=s) for s in (611, 612)]
     for n in ("w13", "w13_s", "w2", "w2_s"):
         wls[1][n] = wls[0][n]
-    layer = _layer(wls[0], cuda)
+    if contiguous:
+        to = lambda t: t.to(cuda)  # noqa: E731
+        layer = B.MoeLayer(T, K, N, E, k, None, to(wls[0]["w13"]), to(wls[0]["w13_s"]),
+                           to(wls[0]["w2"]), to(wls[0]["w2_s"]), device=cuda, contiguous=True)
+    else:
+        layer = _layer(wls[0], cuda)
     s = torch.cuda.Stream()
     outs = []
     for wl in wls:

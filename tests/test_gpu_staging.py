@@ -365,3 +365,39 @@ def test_dispatch_with_eplb_both_paths(cuda, orc, T, K, k, idt, wdt, sf_mode, co
         got_x, got_sf = got_x[rows], got_sf[rows]
     assert np.array_equal(got_x, xr)
     assert np.array_equal(got_sf.view(np.uint32), np.asarray(sfr).view(np.uint32))
+
+
+@pytest.mark.parametrize("T,k,E", [
+    (100, 8, 1000),   # one launch: each scan thread owns four experts, the last three
+    (60, 4, 300),     # one launch: two experts a thread, most threads idle
+])
+def test_small_dispatch_contiguous_many_experts(cuda, orc, T, k, E):
+    """The one-launch dispatch in the contiguous layout with more experts than
+    scan threads: offsets, rows, copied rows and scales bit-exact."""
+    K = 256
+    hid = syn.make_hidden(T, K, 70 + E)
+    ids, w, pad = syn.make_routing(T, E, k, 71 + E, padding_frac=0.05)
+    dev = torch.device("cuda")
+    M_max = (T * k + E - 1) // E
+    rows_cap = E * M_max
+    Wd = (K // 128 + 3) // 4
+    x_b = torch.full((rows_cap, K), 0x5A, dtype=torch.uint8, device=dev)
+    sf_b = torch.full((rows_cap, Wd), -7, dtype=torch.int32, device=dev)
+    ent = torch.full((E,), -1, dtype=torch.int32, device=dev)
+    slot = torch.full((T, k), -9, dtype=torch.int32, device=dev)
+    offs = torch.full((E + 1,), -1, dtype=torch.int32, device=dev)
+    ws = torch.empty(B.prepare_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    disp = dict(num_experts=E, max_tokens_per_expert=M_max, x_b=x_b, sf_b=sf_b,
+                expert_num_tokens=ent, route_slot=slot, workspace=ws, expert_offsets=offs)
+    _, _, _, _, st = _gpu_stage(hid, ids, w, pad, dispatch=disp)
+    assert st == 0
+    ref = orc.prepare_inputs(bf16_bits(hid), ids.numpy(), w.numpy(), is_padding=pad.numpy())
+    d = orc.dispatch_contiguous(ref["ids"], ref["x"], ref["x_sf"], E)
+    assert d["status"] == 0
+    assert np.array_equal(offs.cpu().numpy(), d["expert_offsets"])
+    assert np.array_equal(ent.cpu().numpy(), d["expert_num_tokens"])
+    assert np.array_equal(slot.cpu().numpy(), d["route_row"])
+    n = int(d["expert_offsets"][-1])
+    assert np.array_equal(x_b.cpu().numpy()[:n], d["x_c"][:n])
+    assert np.array_equal(sf_b.cpu().numpy()[:n], d["sf_c"][:n])
+    assert np.all(x_b.cpu().numpy()[n:] == 0x5A)
